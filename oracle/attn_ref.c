@@ -1,0 +1,178 @@
+/*
+ * attn_ref.c -- fp64 CPU oracle for the exact attention forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the test-suite, the smoke check and the CPU-baseline
+ * leg of the benchmark use it.  It shares no code, header, table or constant
+ * with the CUDA library; the two meet only in the seeded inputs they are given.
+ *
+ * What it computes (the plain definition, no tiling, no online rescale):
+ *   for every batch b, query head h and query row i, with kv head h / (Hq/Hkv),
+ *     s_j  = scale * sum_d q[i,d] k[j,d]            for the allowed keys j
+ *     m    = max_j s_j
+ *     l    = sum_j exp(s_j - m)
+ *     P_j  = exp(s_j - m) / l
+ *     O[i] = sum_j P_j v[j]
+ *     LSE  = m + ln l                                 (natural log, scale included)
+ *   Softmax attention is the normaliser whose log-sum-exp has a closed form
+ *   (page "AdaSplash-2: Faster Differentiable Sparse Attention", technical
+ *   summary section 1, problem statement); the fused FlashAttention-style
+ *   kernel (same section) reaches this same result up to rounding order.
+ *   The kernels the article "L'agent a questions depasse l'agent a outils :
+ *   113% contre 50% de la vitesse de FlashAttention-3" reports (section
+ *   "Ce que cela a donne") are attention *forward* kernels checked against an
+ *   fp32 reference (section "Comment une question change la tache"); this
+ *   oracle plays that reference's role, in fp64.
+ *
+ * Readings where the pages say nothing (each listed in the design notes):
+ *   - layout: q,o [B][Hq][Sq][D]; k,v [B][Hkv][Sk][D]; lse [B][Hq][Sq]; contiguous.
+ *   - GQA: query head h reads kv head h / (Hq/Hkv) (contiguous groups).
+ *   - causal = 0: every key allowed; 1: bottom-right aligned, key j allowed for
+ *     row i iff j <= i + (Sk - Sq); 2: top-left aligned, j <= i.
+ *   - a row with no allowed key has O = 0 and LSE = -inf.
+ *   - inputs arrive as raw bf16 bit patterns and are widened exactly; scale is
+ *     the fp32 value the GPU receives, widened exactly to fp64.
+ *
+ * Build: gcc -O2 -fopenmp -shared -fPIC attn_ref.c -o libattn_ref.so -lm
+ * Portable C99: no intrinsics, no architecture flags (runs on x86_64 and aarch64).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Exact widening of a bf16 bit pattern: bf16 is the top half of an fp32. */
+static double bf16_bits_to_f64(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Number of keys row i may attend to (keys 0 .. n-1), per the causal reading above. */
+static int64_t allowed_keys(int64_t i, int64_t Sq, int64_t Sk, int causal) {
+    int64_t last;
+    if (causal == 0) return Sk;
+    last = (causal == 1) ? (i + Sk - Sq) : i;
+    if (last >= Sk) last = Sk - 1;
+    return last < 0 ? 0 : last + 1;
+}
+
+/*
+ * One query row.  s (scratch) and p (optional output) hold at least Sk doubles.
+ * q_row: D bf16; kh, vh: the kv head's [Sk][D] bf16.  Writes o_row[D] and *lse.
+ */
+static void ref_row(const uint16_t* q_row, const uint16_t* kh, const uint16_t* vh,
+                    int64_t i, int64_t Sq, int64_t Sk, int64_t D, int causal, double scale,
+                    double* s, double* p, double* o_row, double* lse) {
+    int64_t n = allowed_keys(i, Sq, Sk, causal);
+    int64_t j, d;
+    double m, l;
+
+    for (d = 0; d < D; ++d) o_row[d] = 0.0;
+    if (p) for (j = 0; j < Sk; ++j) p[j] = 0.0;
+    if (n == 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    /* logits of the allowed keys */
+    for (j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (d = 0; d < D; ++d)
+            acc += bf16_bits_to_f64(q_row[d]) * bf16_bits_to_f64(kh[j * D + d]);
+        s[j] = scale * acc;
+    }
+    /* row maximum and normaliser */
+    m = s[0];
+    for (j = 1; j < n; ++j) if (s[j] > m) m = s[j];
+    l = 0.0;
+    for (j = 0; j < n; ++j) l += exp(s[j] - m);
+    /* probabilities, then the weighted sum of value rows */
+    for (j = 0; j < n; ++j) {
+        double pj = exp(s[j] - m) / l;
+        if (p) p[j] = pj;
+        for (d = 0; d < D; ++d) o_row[d] += pj * bf16_bits_to_f64(vh[j * D + d]);
+    }
+    *lse = m + log(l);
+}
+
+static int check_args(int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return 1;
+    if (Hq % Hkv != 0) return 1;
+    if (causal < 0 || causal > 2) return 1;
+    return 0;
+}
+
+/*
+ * Full or row-subset forward.
+ *   rows == NULL: every row; o is [B][Hq][Sq][D], lse is [B][Hq][Sq].
+ *   rows != NULL: nrows flat row ids r = (b*Hq + h)*Sq + i; o is [nrows][D],
+ *                 lse is [nrows] (compact, in the order given).
+ * Returns 0 on success, 1 on bad arguments, 2 on allocation failure.
+ */
+int attn_ref_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                 double* o, double* lse,
+                 int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                 const int64_t* rows, int64_t nrows) {
+    const int64_t G = (Hkv > 0) ? (int64_t)Hq / Hkv : 1;
+    const int64_t total = (int64_t)B * Hq * Sq;
+    const int64_t count = rows ? nrows : total;
+    const double scale64 = (double)scale;
+    int failed = 0;
+    int64_t t;
+
+    if (check_args(B, Hq, Hkv, Sq, Sk, D, causal)) return 1;
+    if (rows) {
+        for (t = 0; t < nrows; ++t)
+            if (rows[t] < 0 || rows[t] >= total) return 1;
+    }
+
+#pragma omp parallel for schedule(dynamic, 8) reduction(| : failed)
+    for (t = 0; t < count; ++t) {
+        const int64_t r = rows ? rows[t] : t;
+        const int64_t i = r % Sq;
+        const int64_t bh = r / Sq;
+        const int64_t b = bh / Hq, h = bh % Hq;
+        const int64_t kvh = h / G;
+        const uint16_t* kh = k + ((b * Hkv + kvh) * (int64_t)Sk) * D;
+        const uint16_t* vh = v + ((b * Hkv + kvh) * (int64_t)Sk) * D;
+        double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+        if (!s) { failed |= 1; continue; }
+        ref_row(q + r * D, kh, vh, i, Sq, Sk, D, causal, scale64, s, NULL,
+                o + t * D, lse + t);
+        free(s);
+    }
+    return failed ? 2 : 0;
+}
+
+/*
+ * Probability matrix of one (b, h) slice, for pinning the oracle on tiny shapes:
+ * p is [Sq][Sk] (zeros for masked keys), o is [Sq][D], lse is [Sq].  Same row
+ * routine as attn_ref_fwd, so the pins see the code path the comparisons use.
+ */
+int attn_ref_probs(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                   double* p, double* o, double* lse,
+                   int Sq, int Sk, int D, int causal, float scale) {
+    int64_t i;
+    double* s;
+    if (check_args(1, 1, 1, Sq, Sk, D, causal)) return 1;
+    s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+    if (!s) return 2;
+    for (i = 0; i < Sq; ++i)
+        ref_row(q + i * D, k, v, i, Sq, Sk, D, causal, (double)scale, s,
+                p + i * (int64_t)Sk, o + i * D, lse + i);
+    free(s);
+    return 0;
+}
+
+/* Threads the oracle's parallel loop uses (reported beside its timings). */
+int attn_ref_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
