@@ -1,0 +1,56 @@
+"""ctypes loading of the in-tree CUDA libraries (argument marshalling only).
+
+The libraries are built by ``attention_forward_06_gb300.build`` into ``_build/``.
+Loading fails loudly when a library is missing: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_libs: dict[str, ctypes.CDLL] = {}
+
+_c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+
+# name -> (restype, argtypes), mirroring include/attn_fwd.h and include/attn_fwd_probe.h
+SIGNATURES = {
+    "attn_fwd": {
+        "attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
+        "attn_fwd_strerror": (ctypes.c_char_p, [_c_int]),
+        "attn_fwd_version": (_c_int, []),
+        "attn_fwd_debug_status": (_c_int, [_vp, ctypes.POINTER(_c_int)]),
+    },
+    "attn_probe": {
+        "attn_probe_mma_ss": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _vp, _vp]),
+        "attn_probe_mma_ts": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    },
+}
+
+
+class LibraryMissing(RuntimeError):
+    pass
+
+
+def load(name: str = "attn_fwd", build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load ``lib<name>.so`` from ``_build/`` and set its function signatures."""
+    with _lock:
+        if name in _libs:
+            return _libs[name]
+        path = _build.lib_path(name)
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise LibraryMissing(
+                    f"{path} is missing: build it with `python -m attention_forward_06_gb300.build` "
+                    "(the CUDA path has no fallback)")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        for fn, (res, args) in SIGNATURES[name].items():
+            f = getattr(lib, fn)
+            f.restype = res
+            f.argtypes = args
+        _libs[name] = lib
+        return lib

@@ -1,0 +1,565 @@
+// attn_fwd.cu -- exact attention forward pass for GB300 (sm_103a), fused so the
+// Sq x Sk score matrix stays on chip (page "AdaSplash-2: Faster Differentiable
+// Sparse Attention", technical summary section 1: FlashAttention's fused,
+// on-chip softmax attention with a closed-form log-sum-exp normaliser).
+//
+// One CTA owns a work item: 256 query rows (two 128-row Q tiles) of one
+// (batch, query head).  Ten warps, each with one role:
+//   warps 0-3  softmax for Q tile 0 (one thread per query row)
+//   warps 4-7  softmax for Q tile 1
+//   warp  8    TMA producer: Q tiles once, then K/V tiles through a ring of
+//              shared-memory slots guarded by full/empty mbarriers
+//   warp  9    tcgen05 issuer: S_t = Q_t K^T into tensor memory (TMEM), and
+//              O_t += P_t V with P_t read back from TMEM; owns the TMEM allocation
+// The issuer interleaves the two Q tiles so the tensor cores work on one tile
+// while the other tile's softmax runs:
+//   S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
+// TMEM columns: S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [384,384+D); P_t
+// (bf16 pairs) overwrites the first 64 columns of S_t once S_t is in registers.
+//
+// Online softmax per row, in log2 units (c = scale * log2 e): the running max
+// m is only raised when a tile's max exceeds it by more than 8 (a factor 256);
+// otherwise the stale m stays, which is exact because O and the normaliser l
+// share it.  l sums the bf16-rounded P values the tensor cores multiply, so the
+// final O / l is a convex combination of V rows.  Causal masking touches only
+// the tiles that straddle the diagonal (or the ragged end of K); tiles wholly
+// above the diagonal are never loaded.
+//
+// Every mbarrier wait is bounded: a wait that runs out sets a shared abort
+// flag and a device status word, and all roles unwind to the final barrier,
+// the issuer drains its MMAs and the producer its copies before TMEM is freed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn_fwd.h"
+#include "host_util.h"
+#include "ptx.cuh"
+
+using namespace attn;
+
+namespace {
+
+constexpr int BM = 128;          // query rows per Q tile (MMA M)
+constexpr int BN = 128;          // keys per K/V tile
+constexpr int QTILES = 2;        // Q tiles per work item
+constexpr int ROWS_PER_ITEM = QTILES * BM;
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s per wait
+constexpr uint64_t kDrainTimeoutNs = 500000000ull;
+constexpr float kRescaleThreshold = 8.0f;       // log2 units
+
+// Sites recorded in the device status word when a wait runs out.
+constexpr int kSiteProducer = 1;
+constexpr int kSiteIssuer = 2;
+constexpr int kSiteSoftmax = 3;
+constexpr int kSiteEpilogue = 4;
+
+template <int D>
+struct Cfg {
+  static constexpr int kTileBytes = BN * D * 2;            // one K or V tile; also one Q tile
+  static constexpr int kColBlockBytes = BN * 128;          // 64 columns x 128 rows, 128-B swizzled
+  static constexpr int kStages = (D == 128) ? 5 : 8;       // K/V ring slots
+  static constexpr int kQBytes = QTILES * BM * D * 2;
+  static constexpr int kSmemBytes = kQBytes + kStages * kTileBytes + 1024;  // + alignment slack
+};
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  int Hq, Hkv, G, Sq, Sk;
+  int causal;     // 0 none, else key j allowed for row i iff j <= i + diag
+  int diag;
+  int n_qblocks;  // ceil(Sq / ROWS_PER_ITEM)
+  int BH;         // B * Hq
+  float c;        // scale * log2(e)
+};
+
+__device__ int g_status;  // sticky: 0 = fine, else the site of the first wait that ran out
+
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+// Every lane polls; the answer is made warp-uniform so the .sync.aligned
+// tcgen05 instructions that follow are always executed by the whole warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                          uint64_t timeout_ns) {
+  const bool ok = mbar_wait_bounded(bar, parity, abort_flag, timeout_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void record_abort(volatile uint32_t* abort_flag, int site) {
+  *abort_flag = 1;
+  atomicCAS(&g_status, 0, site);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const Params p) {
+  using C = Cfg<D>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  uint8_t* q_s = smem;               // Q tile t at q_s + t * kTileBytes
+  uint8_t* kv_s = smem + C::kQBytes;  // slot s at kv_s + s * kTileBytes
+  __shared__ uint64_t kv_full[S], kv_empty[S];
+  __shared__ uint64_t q_full, s_full[QTILES], p_full[QTILES], o_final;
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ uint32_t abort_flag;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // ---- work item: heaviest query blocks first (they have the most key tiles under a causal mask)
+  const int qb = p.n_qblocks - 1 - static_cast<int>(blockIdx.x) / p.BH;
+  const int bh = static_cast<int>(blockIdx.x) % p.BH;
+  const int b = bh / p.Hq;
+  const int hq = bh % p.Hq;
+  const int kv_z = b * p.Hkv + hq / p.G;
+  const int q0 = qb * ROWS_PER_ITEM;
+  int kv_end = p.Sk;
+  if (p.causal) {
+    const int last_row = min(q0 + ROWS_PER_ITEM, p.Sq) - 1;
+    kv_end = min(p.Sk, last_row + p.diag + 1);
+  }
+  const int n_tiles = kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(&q_full, 1);
+    for (int t = 0; t < QTILES; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4 * 32);
+    }
+    mbar_init(&o_final, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&tmem_base_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_slot;
+  volatile uint32_t* abort_v = &abort_flag;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (n_tiles > 0) {
+      if (lane == 0) {
+        tma_prefetch_map(&tq);
+        tma_prefetch_map(&tk);
+        tma_prefetch_map(&tv);
+        mbar_arrive_expect_tx(&q_full, C::kQBytes);
+        for (int t = 0; t < QTILES; ++t)
+          for (int cb = 0; cb < D / 64; ++cb)
+            tma_load_3d(q_s + t * C::kTileBytes + cb * C::kColBlockBytes, &tq, &q_full, cb * 64, q0 + t * BM, bh);
+      }
+      __syncwarp();
+      int issued = 0;  // K/V tile loads issued so far (K_j is load 2j, V_j is load 2j+1)
+      bool ok = true;
+      for (int it = 0; it < 2 * n_tiles && ok; ++it) {
+        const int slot = it % S;
+        const int use = it / S;
+        if (use > 0) {
+          ok = warp_wait(&kv_empty[slot], (use - 1) & 1, abort_v, kTimeoutNs);
+          if (!ok) {
+            if (lane == 0) record_abort(abort_v, kSiteProducer);
+            break;
+          }
+        }
+        if (lane == 0) {
+          const int j = it >> 1;
+          const CUtensorMap* map = (it & 1) ? &tv : &tk;
+          mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
+          for (int cb = 0; cb < D / 64; ++cb)
+            tma_load_3d(kv_s + slot * C::kTileBytes + cb * C::kColBlockBytes, map, &kv_full[slot], cb * 64,
+                        j * BN, kv_z);
+        }
+        __syncwarp();
+        ++issued;
+      }
+      if (!ok || *abort_v) {
+        // unwinding: let the copies already in flight land before the CTA exits
+        mbar_wait_bounded(&q_full, 0, abort_v, kDrainTimeoutNs);
+        for (int it = (issued > S ? issued - S : 0); it < issued; ++it)
+          mbar_wait_bounded(&kv_full[it % S], (it / S) & 1, abort_v, kDrainTimeoutNs);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ tcgen05 issuer
+    if (n_tiles > 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
+      const uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
+      const uint32_t q_addr = smem_u32(q_s);
+      const uint32_t kv_addr = smem_u32(kv_s);
+      auto issue_s = [=](int t, int slot) {
+        const uint32_t qa = q_addr + t * C::kTileBytes;
+        const uint32_t ka = kv_addr + slot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::kColBlockBytes + (kk % 4) * 32;
+          mma_bf16_ss(tmem + t * BN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s,
+                      kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [=](int t, int slot, bool accumulate) {
+        const uint32_t va = kv_addr + slot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ts(tmem + 2 * BN + t * 128, tmem + t * BN + kk * 8,
+                      sdesc_sw128(va + kk * 16 * 128, C::kColBlockBytes, 1024), idesc_pv,
+                      (accumulate || kk > 0) ? 1u : 0u);
+      };
+      bool ok = warp_wait(&q_full, 0, abort_v, kTimeoutNs);
+      int kslot = 0;
+      if (ok) ok = warp_wait(&kv_full[0], 0, abort_v, kTimeoutNs);
+      if (ok) {
+        tc_fence_after();
+        if (lane == 0) {
+          issue_s(0, kslot);
+          mma_commit(&s_full[0]);
+          issue_s(1, kslot);
+          mma_commit(&s_full[1]);
+          mma_commit(&kv_empty[kslot]);
+        }
+        __syncwarp();
+      }
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int vit = 2 * j + 1;
+        const int vslot = vit % S;
+        ok = warp_wait(&kv_full[vslot], (vit / S) & 1, abort_v, kTimeoutNs);
+        if (ok) ok = warp_wait(&p_full[0], j & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) issue_pv(0, vslot, j > 0);
+        __syncwarp();
+        const bool more = j + 1 < n_tiles;
+        if (more) {
+          const int kit = 2 * j + 2;
+          kslot = kit % S;
+          ok = warp_wait(&kv_full[kslot], (kit / S) & 1, abort_v, kTimeoutNs);
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            issue_s(0, kslot);
+            mma_commit(&s_full[0]);
+          }
+          __syncwarp();
+        }
+        ok = warp_wait(&p_full[1], j & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_pv(1, vslot, j > 0);
+          mma_commit(&kv_empty[vslot]);
+          if (more) {
+            issue_s(1, kslot);
+            mma_commit(&s_full[1]);
+            mma_commit(&kv_empty[kslot]);
+          }
+        }
+        __syncwarp();
+      }
+      if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
+      // o_final: every MMA issued above has completed (also the drain before TMEM is freed)
+      if (lane == 0) mma_commit(&o_final);
+      __syncwarp();
+      warp_wait(&o_final, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (+ rescale, epilogue)
+    const int t = warp / 4;
+    const int quarter = warp % 4;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_off + t * BN;
+    const uint32_t o_tmem = tmem + lane_off + 2 * BN + t * 128;
+    const int row = q0 + t * BM + quarter * 32 + lane;  // global query row
+    const int tile_row0 = q0 + t * BM;
+    // last allowed key of this row, and of the tile's first row (the most restricted)
+    int lim = p.Sk - 1, lim_tile = p.Sk - 1;
+    if (p.causal) {
+      lim = min(lim, row + p.diag);
+      lim_tile = min(lim_tile, tile_row0 + p.diag);
+    }
+    const float c = p.c;
+    float m = -INFINITY;  // running max, log2 units
+    float l = 0.0f;       // running normaliser at max m
+    bool ok = true;
+
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = warp_wait(&s_full[t], j & 1, abort_v, kTimeoutNs);
+      if (!ok) {
+        if (lane == 0) record_abort(abort_v, kSiteSoftmax);
+        break;
+      }
+      tc_fence_after();
+      uint32_t r[128];
+      tmem_ld128_wait(s_tmem, r);
+      float s[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
+      if (j * BN + BN - 1 > lim_tile) {  // tile straddles the diagonal or the end of K
+        const int kmax = lim - j * BN;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = (i > kmax) ? -INFINITY : s[i];
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      const float m_tile = mx * c;
+      const bool raise = m_tile > m + kRescaleThreshold;
+      float alpha = 1.0f;
+      if (raise) {
+        alpha = ex2_approx(m - m_tile);
+        m = m_tile;
+        l *= alpha;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, raise)) {
+        // rescale this warp's 32 rows of O_t (PV_t(j-1) has completed: its commit preceded S_t(j)'s)
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t o[32];
+          tmem_ld32_wait(o_tmem + cb * 32, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(o_tmem + cb * 32, o);
+        }
+      }
+      const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2_approx(fmaf(s[half * 64 + 2 * i], c, neg_m));
+          const float p1 = ex2_approx(fmaf(s[half * 64 + 2 * i + 1], c, neg_m));
+          pk[i] = pack_bf16x2(p0, p1);
+          l += bf16lo_to_f32(pk[i]) + bf16hi_to_f32(pk[i]);
+        }
+        tmem_st32(s_tmem + half * 32, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full[t]);
+    }
+
+    // ---- epilogue: O = O_acc / l in bf16, LSE = (m + log2 l) * ln 2
+    bool have_o = false;
+    const bool aborted = __any_sync(0xffffffffu, *abort_v != 0);  // warp-uniform view of the flag
+    if (n_tiles > 0 && ok && !aborted) {
+      have_o = warp_wait(&o_final, 0, abort_v, kTimeoutNs);
+      if (!have_o) {
+        if (lane == 0) record_abort(abort_v, kSiteEpilogue);
+      } else {
+        tc_fence_after();
+      }
+    }
+    const bool live = row < p.Sq;
+    const bool any_key = have_o && l > 0.0f;
+    const float inv_l = any_key ? 1.0f / l : 0.0f;
+    __nv_bfloat16* orow = p.o + (static_cast<int64_t>(bh) * p.Sq + row) * D;
+    if (have_o) {
+      __syncwarp();
+#pragma unroll
+      for (int cb = 0; cb < D / 32; ++cb) {
+        uint32_t o[32];
+        tmem_ld32_wait(o_tmem + cb * 32, o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+    } else if (live && !aborted) {
+      uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+      for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (live && (have_o || !aborted)) {
+      const float lse = any_key ? (m + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+      p.lse[static_cast<int64_t>(bh) * p.Sq + row] = lse;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = e;
+  return ATTN_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+int g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 unsupported
+
+// Capability check and kernel attributes, once per device.
+int prepare_device(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_dev_state[dev] == 1) return ATTN_OK;
+  if (g_dev_state[dev] == -1) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  int major = 0, minor = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (major != 10 || minor != 3) {
+    g_dev_state[dev] = -1;
+    return ATTN_ERR_UNSUPPORTED_DEVICE;
+  }
+  e = cudaFuncSetAttribute(attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128>::kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<64>::kSmemBytes);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (!attn_host::encode_tiled_fn()) return ATTN_ERR_TENSOR_MAP;
+  g_dev_state[dev] = 1;
+  return ATTN_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+template <int D>
+int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const Params& prm, int grid,
+           cudaStream_t stream) {
+  attn_fwd_kernel<D><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, prm);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+             int Sk, int D, int causal, float scale, cudaStream_t stream) {
+  // ---- argument checks (host only, before any CUDA call)
+  if (B < 0 || Sq < 0 || Sk < 0 || Hq < 1 || Hkv < 1) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal < 0 || causal > 2) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  const int64_t q_elems = static_cast<int64_t>(B) * Hq * Sq * D;
+  const int64_t kv_elems = static_cast<int64_t>(B) * Hkv * Sk * D;
+  const int64_t rows = static_cast<int64_t>(B) * Hq * Sq;
+  if (static_cast<int64_t>(B) * Hq > INT32_MAX || static_cast<int64_t>(B) * Hkv > INT32_MAX)
+    return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0) return ATTN_OK;  // nothing to compute
+  const int64_t n_qblocks = (Sq + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM;
+  const int64_t grid64 = static_cast<int64_t>(B) * Hq * n_qblocks;
+  if (grid64 > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+  if (!q || !o || !lse) return ATTN_ERR_NULL_PTR;
+  if (Sk > 0 && (!k || !v)) return ATTN_ERR_NULL_PTR;
+  auto misaligned = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+  if (misaligned(q) || misaligned(o) || misaligned(lse)) return ATTN_ERR_MISALIGNED;
+  if (Sk > 0 && (misaligned(k) || misaligned(v))) return ATTN_ERR_MISALIGNED;
+  const size_t qb = static_cast<size_t>(q_elems) * 2, kvb = static_cast<size_t>(kv_elems) * 2;
+  const size_t lb = static_cast<size_t>(rows) * 4;
+  if (overlaps(o, qb, q, qb) || overlaps(o, qb, k, kvb) || overlaps(o, qb, v, kvb) || overlaps(o, qb, lse, lb) ||
+      overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kvb) || overlaps(lse, lb, v, kvb))
+    return ATTN_ERR_INVALID_ARG;
+
+  // ---- device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int st = prepare_device(dev);
+  if (st != ATTN_OK) return st;
+
+  // ---- TMA maps: Q [B*Hq][Sq][D], K/V [B*Hkv][Sk][D]; boxes of 64 columns x 128 rows
+  CUtensorMap tq, tk, tv;
+  if (!attn_host::encode_bf16_rows(&tq, q, D, Sq, static_cast<uint64_t>(B) * Hq, BM)) return ATTN_ERR_TENSOR_MAP;
+  if (Sk > 0) {
+    if (!attn_host::encode_bf16_rows(&tk, k, D, Sk, static_cast<uint64_t>(B) * Hkv, BN)) return ATTN_ERR_TENSOR_MAP;
+    if (!attn_host::encode_bf16_rows(&tv, v, D, Sk, static_cast<uint64_t>(B) * Hkv, BN)) return ATTN_ERR_TENSOR_MAP;
+  } else {
+    tk = tq;  // never read: every row is fully masked and no key tile is loaded
+    tv = tq;
+  }
+
+  Params prm;
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.G = Hq / Hkv;
+  prm.Sq = Sq;
+  prm.Sk = Sk;
+  prm.causal = causal != 0;
+  prm.diag = causal == 1 ? Sk - Sq : 0;
+  prm.n_qblocks = static_cast<int>(n_qblocks);
+  prm.BH = B * Hq;
+  prm.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  const int grid = static_cast<int>(grid64);
+  return D == 128 ? launch<128>(tq, tk, tv, prm, grid, stream) : launch<64>(tq, tk, tv, prm, grid, stream);
+}
+
+const char* attn_fwd_strerror(int status) {
+  switch (status) {
+    case ATTN_OK: return "success";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_NULL_PTR: return "null pointer";
+    case ATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case ATTN_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+    case ATTN_ERR_CUDA: return cudaGetErrorString(t_last_cuda_error);
+    case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel wait ran out of time; the kernel unwound";
+    case ATTN_ERR_TENSOR_MAP: return "TMA tensor map rejected by the driver";
+    default: return "unknown status";
+  }
+}
+
+int attn_fwd_version(void) { return 100; }  // 0.1.0
+
+int attn_fwd_debug_status(cudaStream_t stream, int* site) {
+  if (site) *site = 0;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int value = 0;
+  e = cudaMemcpyFromSymbol(&value, g_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (value != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (site) *site = value;
+  return value == 0 ? ATTN_OK : ATTN_ERR_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"

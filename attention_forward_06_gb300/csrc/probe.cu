@@ -1,0 +1,208 @@
+// probe.cu -- primitive kernels that check, one building block at a time, the
+// hand-encoded pieces the attention kernel is made of:
+//   * a TMA tile load with 128-byte swizzle and zero fill past the last row;
+//   * S = Q K^T with both operands K-major in shared memory (SS form), the
+//     accumulator read back from tensor memory with tcgen05.ld;
+//   * O = P V with P written into tensor memory by tcgen05.st (TS form) and V
+//     MN-major in shared memory.
+// Each runs as a single CTA of 128 threads on one 128-row tile; the tests
+// compare the results with CPU matmuls.  Test infrastructure for the library
+// (declared in include/attn_fwd_probe.h), not part of the attention path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "host_util.h"
+#include "ptx.cuh"
+
+using namespace attn;
+
+namespace {
+
+constexpr uint64_t kProbeTimeoutNs = 2000000000ull;  // 2 s
+constexpr int kTile = 128;
+
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+// q_rows/k_rows < 128 exercise the zero fill of rows past the end.
+__global__ void __launch_bounds__(128, 1)
+    probe_mma_ss_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk, int D,
+                        float* s_out, uint16_t* q_dump, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  uint8_t* q_s = smem;
+  uint8_t* k_s = smem + kTile * D * 2;
+  __shared__ uint64_t bar_load, bar_mma;
+  __shared__ uint32_t tmem_base;
+  __shared__ uint32_t abort_flag;
+  const int warp = threadIdx.x / 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_load, 1);
+    mbar_init(&bar_mma, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bar_load, 2u * kTile * D * 2);
+    for (int c = 0; c < D / 64; ++c) {
+      tma_load_3d(q_s + c * kTile * 128, &tq, &bar_load, c * 64, 0, 0);
+      tma_load_3d(k_s + c * kTile * 128, &tk, &bar_load, c * 64, 0, 0);
+    }
+    if (mbar_wait_bounded(&bar_load, 0, &abort_flag, kProbeTimeoutNs)) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16_f32(128, 128, false);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
+        mma_bf16_ss(tbase, sdesc_sw128(smem_u32(q_s) + off, 16, 1024), sdesc_sw128(smem_u32(k_s) + off, 16, 1024),
+                    idesc, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(&bar_mma);
+    } else {
+      abort_flag = 1;
+      atomicExch(status, 1);
+    }
+  }
+  const bool ok = mbar_wait_bounded(&bar_mma, 0, &abort_flag, kProbeTimeoutNs);
+  tc_fence_after();
+  if (ok) {
+    const int row = threadIdx.x;
+    for (int c = 0; c < 4; ++c) {
+      uint32_t r[32];
+      tmem_ld32_wait(tbase + (static_cast<uint32_t>(warp * 32) << 16) + c * 32, r);
+      for (int i = 0; i < 32; ++i) s_out[row * kTile + c * 32 + i] = __uint_as_float(r[i]);
+    }
+  } else if (threadIdx.x == 0) {
+    atomicExch(status, 2);
+  }
+  const uint16_t* qh = reinterpret_cast<const uint16_t*>(q_s);
+  for (int i = threadIdx.x; i < kTile * D; i += blockDim.x) q_dump[i] = qh[i];
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 128);
+  }
+}
+
+// p: [128][128] bf16 row-major (row = query, column = key); v via map [128][D].
+__global__ void __launch_bounds__(128, 1)
+    probe_mma_ts_kernel(const __grid_constant__ CUtensorMap tv, const uint32_t* p, int D, uint32_t lbo, uint32_t sbo,
+                        float* o_out, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* v_s = align_1024(smem_raw);
+  __shared__ uint64_t bar_load, bar_mma;
+  __shared__ uint32_t tmem_base;
+  __shared__ uint32_t abort_flag;
+  const int warp = threadIdx.x / 32;
+  const int row = threadIdx.x;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_load, 1);
+    mbar_init(&bar_mma, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+  // P row -> TMEM columns [0, 64): two bf16 per 32-bit column.
+  for (int c = 0; c < 2; ++c) {
+    uint32_t r[32];
+    for (int i = 0; i < 32; ++i) r[i] = p[row * 64 + c * 32 + i];
+    tmem_st32(tbase + lane_base + c * 32, r);
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  __syncthreads();
+
+  if (threadIdx.x == 0) {
+    tc_fence_after();
+    mbar_arrive_expect_tx(&bar_load, static_cast<uint32_t>(kTile * D * 2));
+    for (int c = 0; c < D / 64; ++c) tma_load_3d(v_s + c * kTile * 128, &tv, &bar_load, c * 64, 0, 0);
+    if (mbar_wait_bounded(&bar_load, 0, &abort_flag, kProbeTimeoutNs)) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16_f32(128, D, true);
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_bf16_ts(tbase + 128, tbase + kk * 8, sdesc_sw128(smem_u32(v_s) + kk * 16 * 128, lbo, sbo), idesc,
+                    kk > 0 ? 1u : 0u);
+      mma_commit(&bar_mma);
+    } else {
+      abort_flag = 1;
+      atomicExch(status, 1);
+    }
+  }
+  const bool ok = mbar_wait_bounded(&bar_mma, 0, &abort_flag, kProbeTimeoutNs);
+  tc_fence_after();
+  if (ok) {
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32_wait(tbase + lane_base + 128 + c * 32, r);
+      for (int i = 0; i < 32; ++i) o_out[row * D + c * 32 + i] = __uint_as_float(r[i]);
+    }
+  } else if (threadIdx.x == 0) {
+    atomicExch(status, 2);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 256);
+  }
+}
+
+int launch_status(cudaError_t e) { return e == cudaSuccess ? 0 : 100 + static_cast<int>(e); }
+
+}  // namespace
+
+extern "C" {
+
+int attn_probe_mma_ss(const void* q, int q_rows, const void* k, int k_rows, int D, float* s_out, void* q_dump,
+                      int* status, cudaStream_t stream) {
+  if (!q || !k || !s_out || !q_dump || !status) return 2;
+  if ((D != 64 && D != 128) || q_rows < 1 || q_rows > kTile || k_rows < 1 || k_rows > kTile) return 1;
+  CUtensorMap tq, tk;
+  if (!attn_host::encode_bf16_rows(&tq, q, D, q_rows, 1, kTile)) return 3;
+  if (!attn_host::encode_bf16_rows(&tk, k, D, k_rows, 1, kTile)) return 3;
+  const int smem = 2 * kTile * D * 2 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(probe_mma_ss_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return launch_status(e);
+  probe_mma_ss_kernel<<<1, 128, smem, stream>>>(tq, tk, D, s_out, static_cast<uint16_t*>(q_dump), status);
+  return launch_status(cudaGetLastError());
+}
+
+int attn_probe_mma_ts(const void* p, const void* v, int D, int lbo, int sbo, float* o_out, int* status,
+                      cudaStream_t stream) {
+  if (!p || !v || !o_out || !status) return 2;
+  if (D != 64 && D != 128) return 1;
+  if (lbo < 0 || sbo < 0 || lbo > 65535 || sbo > 65535 || (lbo % 16) || (sbo % 16)) return 1;
+  CUtensorMap tv;
+  if (!attn_host::encode_bf16_rows(&tv, v, D, kTile, 1, kTile)) return 3;
+  const int smem = kTile * D * 2 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(probe_mma_ts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return launch_status(e);
+  probe_mma_ts_kernel<<<1, 128, smem, stream>>>(tv, static_cast<const uint32_t*>(p), D, static_cast<uint32_t>(lbo),
+                                                static_cast<uint32_t>(sbo), o_out, status);
+  return launch_status(cudaGetLastError());
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+"""Python binding of the C ABI (include/attn_fwd.h): marshals torch tensors into
+pointers and sizes and calls the CUDA library.  Every step of the attention
+computation runs in the library's kernel; torch only provides device memory and
+streams here.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from ._lib import load
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_NULL_PTR = 2
+ATTN_ERR_MISALIGNED = 3
+ATTN_ERR_UNSUPPORTED_DEVICE = 4
+ATTN_ERR_CUDA = 5
+ATTN_ERR_DEVICE_TIMEOUT = 6
+ATTN_ERR_TENSOR_MAP = 7
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"attn_fwd status {status}: {message}")
+        self.status = status
+
+
+def _check(status: int) -> None:
+    if status != ATTN_OK:
+        msg = load().attn_fwd_strerror(status).decode()
+        raise AttnError(status, msg)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, Hq: int, Hkv: int,
+                 Sq: int, Sk: int, D: int, causal: int, scale: float, stream: int) -> int:
+    """Direct call of the C entry point with integer pointers; returns the status code."""
+    return load().attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Sq, Sk, D, causal,
+                           ctypes.c_float(scale), stream)
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: int = 1, scale: float | None = None,
+             o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """Exact attention forward: returns ``(o, lse)``.
+
+    q ``[B,Hq,Sq,D]``, k/v ``[B,Hkv,Sk,D]``: contiguous bf16 CUDA tensors.  ``causal`` is
+    0 (none), 1 (bottom-right aligned) or 2 (top-left aligned).  ``scale`` defaults to
+    1/sqrt(D).  ``o``/``lse`` may be given (``[B,Hq,Sq,D]`` bf16, ``[B,Hq,Sq]`` fp32) to
+    avoid allocation.  Asynchronous on ``stream`` (default: torch's current stream).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-d bf16 CUDA tensor")
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if o.shape != q.shape or o.dtype != torch.bfloat16 or not o.is_contiguous():
+        raise ValueError("o must be a contiguous bf16 tensor shaped like q")
+    if tuple(lse.shape) != (B, Hq, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, Hq, Sq]")
+    _check(attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        B, Hq, Hkv, Sq, Sk, D, int(causal), float(scale), _stream_handle(stream)))
+    return o, lse
+
+
+def debug_status(stream=None) -> tuple[int, int]:
+    """Synchronise ``stream`` and read/clear the kernel's timeout word: ``(status, site)``."""
+    site = ctypes.c_int(0)
+    st = load().attn_fwd_debug_status(_stream_handle(stream), ctypes.byref(site))
+    return st, site.value
+
+
+def version() -> int:
+    return int(load().attn_fwd_version())

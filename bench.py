@@ -1,0 +1,396 @@
+#!/usr/bin/env python
+"""Benchmark of the exact attention forward pass on GB300: prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one call of the fused kernel (every step of the hot path: tile
+scheduling, TMA loads, QK^T, online softmax, rescale, PV, epilogue) over one
+batch of the workload.  ``value`` is attention-forward TFLOPS counted on the
+algorithmic work, 4*D FLOP per unmasked (query, key) pair summed over all
+heads and rows, over the max-over-ranks device time of K steps, with the
+inputs resident in HBM and L2 flushed between steps.  ``e2e`` is the same
+metric through the public API with the step's inputs copied from pinned host
+memory and its outputs copied back inside the timed region.
+
+Under torchrun each rank runs its own copy of the workload on its own GPU
+(independent problems, no collective on the data path: weak scaling).
+``--impl reference`` times the fp64 CPU oracle, as it stands, on a bounded
+sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from attention_forward_06_gb300.inputs import WORKLOADS, Workload, bf16_bits, draw_workload, sample_rows  # noqa: E402
+
+METRIC = "attn fwd TFLOPS (bf16, 1×GB300) and % of dense-BF16 tensor peak; geomean"
+PERF_WORKLOADS = ["train", "gqa", "chunked128", "chunked64", "long"]
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+KERNEL_SOURCES = ["attention_forward_06_gb300/csrc/attn_fwd.cu", "attention_forward_06_gb300/csrc/ptx.cuh"]
+
+
+# ----------------------------------------------------------------------------- work accounting
+def allowed_pairs(w: Workload) -> int:
+    """Unmasked (query row, key) pairs of one (batch, head)."""
+    if w.causal == 0:
+        return w.Sq * w.Sk
+    i = np.arange(w.Sq, dtype=np.int64)
+    last = i + (w.Sk - w.Sq if w.causal == 1 else 0)
+    return int(np.clip(last + 1, 0, w.Sk).sum())
+
+
+def alg_flops(w: Workload) -> float:
+    return 4.0 * w.D * w.B * w.Hq * allowed_pairs(w)
+
+
+def conv_flops(w: Workload) -> float:
+    return 4.0 * w.B * w.Hq * w.Sq * w.Sk * w.D * (0.5 if w.causal else 1.0)
+
+
+def min_hbm_bytes(w: Workload) -> int:
+    return 2 * w.B * (w.Hq * w.Sq * w.D * 2 + w.Hkv * w.Sk * w.D) + 4 * w.B * w.Hq * w.Sq
+
+
+def row_flops(w: Workload, rows: np.ndarray) -> float:
+    i = rows % w.Sq
+    if w.causal == 0:
+        n = np.full(i.shape, w.Sk)
+    else:
+        n = np.clip(i + (w.Sk - w.Sq if w.causal == 1 else 0) + 1, 0, w.Sk)
+    return float(4.0 * w.D * n.sum())
+
+
+# ----------------------------------------------------------------------------- peaks, clocks
+def measured_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- timing
+def time_kernel(fn, steps: int, warmup: int, flush: torch.Tensor, stream) -> list[float]:
+    """Per-step kernel time (ms) with CUDA events on the launching stream; L2 flushed before each step."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def traffic_for(workload: str):
+    """DRAM bytes per launch from a committed ncu capture, or None if absent or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for src in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    entry = rec.get(workload)
+    if not entry or entry.get("kernel_sha256") != h.hexdigest():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def cpu_baseline(w: Workload, budget_s: float = 12.0) -> dict:
+    """The oracle, as it stands, on sampled rows of the workload, for about budget_s seconds."""
+    import oracle  # test infrastructure: timed here as the CPU baseline only
+
+    q, k, v = draw_workload(w)
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    flops, elapsed, nrows, chunk = 0.0, 0.0, 0, 1
+    seed = w.seed + 2000
+    while elapsed < budget_s:
+        rows = sample_rows(w.B, w.Hq, w.Sq, chunk, seed=seed)
+        seed += 1
+        t0 = time.perf_counter()
+        oracle.attention(qb, kb, vb, w.causal, w.scale, rows=rows)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        flops += row_flops(w, rows)
+        nrows += len(rows)
+        if dt < budget_s / 8:
+            chunk = min(chunk * 2, w.Sq)
+    return {"value": flops / elapsed / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{nrows} query rows drawn uniformly per (batch, head) of the {w.name} workload "
+                      f"({flops:.3g} FLOP, {elapsed:.1f} s, fp64)"}
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, w: Workload, rank: int, world: int):
+    if rank != 0:
+        return None
+    import oracle
+
+    q, k, v = draw_workload(w)
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    per_head = max(1, 4096 // (w.B * w.Hq))  # bounded sample per step
+    times, flops = [], []
+    for step in range(args.warmup + args.steps):
+        rows = sample_rows(w.B, w.Hq, w.Sq, per_head, seed=w.seed + 3000 + step)
+        t0 = time.perf_counter()
+        oracle.attention(qb, kb, vb, w.causal, w.scale, rows=rows)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            flops.append(row_flops(w, rows))
+    value = sum(flops) / sum(times) / 1e12
+    sample = f"{per_head} query rows per (batch, head) per step, {w.name} workload, fp64 oracle"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.label(), "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_ours(args, w: Workload, rank: int, world: int, dist):
+    from attention_forward_06_gb300 import ops
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+    q, k, v = draw_workload(w)
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    qd, kd, vd = qh.to(dev), kh.to(dev), vh.to(dev)
+    od = torch.empty_like(qd)
+    lsed = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    oh = torch.empty(od.shape, dtype=od.dtype, pin_memory=True)
+    lseh = torch.empty(lsed.shape, dtype=lsed.dtype, pin_memory=True)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        ops.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, o=od, lse=lsed, stream=stream)
+
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    times = time_kernel(step, args.steps, 0, flush, stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    st, site = ops.debug_status(stream)
+    if st != ops.ATTN_OK:
+        raise RuntimeError(f"kernel wait ran out (site {site})")
+    total_ms = sum(times)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flops = alg_flops(w)
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs -> HBM -> kernel -> host outputs
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        ops.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, o=od, lse=lsed, stream=stream)
+        oh.copy_(od, non_blocking=True)
+        lseh.copy_(lsed, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lseh.numel() * lseh.element_size()
+
+    if rank != 0:
+        return None
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (statistics.mean(times) * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.label(), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
+                   "causal": w.causal, "flop_count": "algorithmic: 4*D per unmasked (row, key) pair",
+                   "alg_flop_per_step": flops, "conv_flop_per_step": conv_flops(w),
+                   "tflops_conv": world * conv_flops(w) * args.steps / (total_ms * 1e-3) / 1e12,
+                   "pct_of_peak": 100.0 * achieved / peak,
+                   "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} bf16_tflops (burst: kernel timed alone)",
+                     "traffic": traffic_for(w.name), "alg_hbm_bytes": min_hbm_bytes(w)},
+        "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.skip_workloads:
+        per = {}
+        for name in PERF_WORKLOADS:
+            if name == w.name:
+                per[name] = achieved
+                continue
+            wx = WORKLOADS[name]
+            qx, kx, vx = [t.to(dev) for t in draw_workload(wx)]
+            ox = torch.empty_like(qx)
+            lx = torch.empty((wx.B, wx.Hq, wx.Sq), dtype=torch.float32, device=dev)
+
+            def fx():
+                ops.attn_fwd(qx, kx, vx, causal=wx.causal, scale=wx.scale, o=ox, lse=lx, stream=stream)
+
+            tx = time_kernel(fx, min(args.steps, 10), 2, flush, stream)
+            per[name] = alg_flops(wx) / (statistics.mean(tx) * 1e-3) / 1e12
+            del qx, kx, vx, ox, lx
+        line["per_workload_tflops"] = per
+        line["geomean_tflops"] = math.exp(sum(math.log(x) for x in per.values()) / len(per))
+        line["geomean_pct_of_peak"] = 100.0 * line["geomean_tflops"] / peak
+    if world == 1 and not args.skip_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="train", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-workloads", action="store_true", help="time only --workload, not the geomean set")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        if args.impl == "reference" and rank != 0:
+            return 0
+        if args.impl == "ours":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            tdist.init_process_group("nccl")
+            dist = tdist
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        line = run_reference(args, w, rank, world)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a GPU for --impl ours (the CUDA path has no CPU fallback)")
+        line = run_ours(args, w, rank, world, dist)
+    if line is not None and rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

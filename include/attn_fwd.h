@@ -1,0 +1,95 @@
+/*
+ * attn_fwd.h -- C ABI of the exact attention forward pass for GB300 (sm_103a).
+ *
+ * Operation.  For every batch b, query head h and query row i:
+ *     O[b,h,i,:] = sum_j P_ij V[b,g(h),j,:],   P_ij = exp(s_ij - LSE_i),
+ *     s_ij       = scale * <Q[b,h,i,:], K[b,g(h),j,:]>   over the allowed keys j,
+ *     LSE[b,h,i] = ln sum_j exp(s_ij)                    (natural log, scale included),
+ * with g(h) = h / (Hq / Hkv) (grouped-query attention: consecutive query heads
+ * share a key/value head).  This is softmax attention with its closed-form
+ * log-sum-exp normaliser (page "AdaSplash-2: Faster Differentiable Sparse
+ * Attention", technical summary section 1), computed fused in the
+ * FlashAttention manner (same section: fused operations kept in on-chip
+ * memory), so the Sq x Sk score matrix never reaches HBM.  It is the attention
+ * forward pass whose hand-written single-file CUDA kernels the article "L'agent
+ * a questions depasse l'agent a outils : 113% contre 50% de la vitesse de
+ * FlashAttention-3" reports for Hopper and Blackwell (section "Ce que cela a
+ * donne").
+ *
+ * Masks (`causal`):
+ *     0  every key is allowed;
+ *     1  bottom-right aligned: key j is allowed for row i iff j <= i + (Sk - Sq)
+ *        (for Sq == Sk this is the usual top-left causal mask);
+ *     2  top-left aligned: key j is allowed for row i iff j <= i.
+ *     A row with no allowed key gets O = 0 and LSE = -inf.
+ *
+ * Layout (all contiguous, row-major, device memory):
+ *     q [B][Hq][Sq][D] bf16     k, v [B][Hkv][Sk][D] bf16
+ *     o [B][Hq][Sq][D] bf16     lse  [B][Hq][Sq] fp32
+ * D must be 64 or 128; Hq must be a multiple of Hkv; every pointer must be
+ * 16-byte aligned.  o and lse must not overlap q, k, v or each other.
+ *
+ * Ownership and execution.  The caller owns every buffer.  attn_fwd allocates
+ * no device memory; it enqueues one kernel on `stream` (0 = legacy default
+ * stream) and returns without synchronising, so errors raised while the kernel
+ * runs surface on the stream (or through attn_fwd_debug_status).  Inputs are
+ * not modified.  Calls are re-entrant; the one-time initialisation (driver
+ * entry point, per-device capability check and kernel attributes) is guarded.
+ *
+ * Precision.  bf16 inputs; both products accumulate in fp32 on the tensor
+ * cores; softmax in fp32 with exp2; P is rounded to bf16 before the P.V
+ * product and the normaliser sums those same rounded values; O is rounded to
+ * bf16 (nearest-even) once, at the end.
+ */
+#ifndef ATTN_FWD_H
+#define ATTN_FWD_H
+
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes (0 = success). */
+#define ATTN_OK 0
+#define ATTN_ERR_INVALID_ARG 1        /* a size < 0, Hq or Hkv < 1, D not 64/128, Hq % Hkv, causal not 0..2,
+                                         overlapping outputs, or a size beyond the 32-bit index range */
+#define ATTN_ERR_NULL_PTR 2           /* a required pointer is NULL */
+#define ATTN_ERR_MISALIGNED 3         /* a pointer is not 16-byte aligned */
+#define ATTN_ERR_UNSUPPORTED_DEVICE 4 /* the current device is not compute capability 10.3 (sm_103a) */
+#define ATTN_ERR_CUDA 5               /* a CUDA runtime call failed; see attn_fwd_strerror(ATTN_ERR_CUDA) */
+#define ATTN_ERR_DEVICE_TIMEOUT 6     /* a kernel wait ran out of time and the kernel unwound (debug status) */
+#define ATTN_ERR_TENSOR_MAP 7         /* the driver rejected a TMA tensor map for these pointers and sizes */
+
+/*
+ * Enqueue the attention forward pass on `stream`.
+ * Returns ATTN_OK or one of the codes above.  Argument checks run on the host
+ * before any device work; nothing is launched when a check fails.  With
+ * B == 0 or Sq == 0 there is nothing to compute and the call returns ATTN_OK
+ * without launching.  Sk == 0 is valid: every row is fully masked.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+             int Sk, int D, int causal, float scale, cudaStream_t stream);
+
+/* Text for a status code.  For ATTN_ERR_CUDA it names the CUDA error of the
+   calling thread's most recent failing call. */
+const char* attn_fwd_strerror(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int attn_fwd_version(void);
+
+/*
+ * Synchronise `stream`, then read and clear the library's device status word
+ * for the current device.  Every wait inside the kernel is bounded (a few
+ * seconds); a wait that runs out records where it gave up and the kernel
+ * unwinds cleanly instead of hanging.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT,
+ * or ATTN_ERR_CUDA when the synchronisation itself reports an error.
+ * `site` (may be NULL) receives the recorded code (0 when none).
+ */
+int attn_fwd_debug_status(cudaStream_t stream, int* site);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FWD_H */

@@ -1,0 +1,123 @@
+"""The C-ABI boundary on the host (no GPU needed): the libraries build for
+sm_103a, load, export every symbol the headers declare, and reject bad
+arguments with the documented status codes before touching any device.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from attention_forward_06_gb300 import build as B
+from attention_forward_06_gb300 import _lib, ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = {"attn_fwd": "include/attn_fwd.h", "attn_probe": "include/attn_fwd_probe.h"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    return B.build()
+
+
+def declared_functions(header):
+    text = open(os.path.join(ROOT, header)).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.mark.parametrize("name", sorted(HEADERS))
+def test_library_exports_every_declared_symbol(name, built):
+    funcs = declared_functions(HEADERS[name])
+    assert funcs, "no declarations parsed"
+    lib = ctypes.CDLL(built[name])
+    for f in funcs:
+        assert hasattr(lib, f), f"{f} declared in {HEADERS[name]} but not exported"
+    # and the Python binding knows exactly these signatures
+    assert sorted(_lib.SIGNATURES[name]) == funcs
+
+
+def test_library_is_built_for_sm_103a_only(built):
+    log = open(os.path.join(B.BUILD_DIR, "attn_fwd.ptxas.log")).read()
+    assert "arch=compute_103a,code=sm_103a" in log
+    assert "for 'sm_103a'" in log
+    assert "sm_90" not in log and "sm_100" not in log
+
+
+def test_version_and_strerror():
+    lib = _lib.load()
+    assert lib.attn_fwd_version() >= 100
+    for code in range(0, 8):
+        assert lib.attn_fwd_strerror(code)
+    assert lib.attn_fwd_strerror(999) == b"unknown status"
+
+
+# fake, 16-byte aligned addresses: validation never dereferences them
+Q, K, V, O, L = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000
+GOOD = dict(B=1, Hq=4, Hkv=2, Sq=64, Sk=64, D=128, causal=1, scale=0.1)
+
+
+def call(q=Q, k=K, v=V, o=O, lse=L, **kw):
+    a = dict(GOOD)
+    a.update(kw)
+    return ops.attn_fwd_raw(q, k, v, o, lse, a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"], a["D"], a["causal"],
+                            a["scale"], 0)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(D=96), dict(D=0), dict(D=256), dict(Hq=3, Hkv=2), dict(Hkv=0), dict(Hq=0), dict(causal=3),
+    dict(causal=-1), dict(B=-1), dict(Sq=-5), dict(Sk=-1), dict(scale=float("nan")), dict(scale=float("inf")),
+])
+def test_invalid_arguments(kw):
+    assert call(**kw) == ops.ATTN_ERR_INVALID_ARG
+
+
+def test_null_pointers():
+    assert call(q=0) == ops.ATTN_ERR_NULL_PTR
+    assert call(k=0) == ops.ATTN_ERR_NULL_PTR
+    assert call(v=0) == ops.ATTN_ERR_NULL_PTR
+    assert call(o=0) == ops.ATTN_ERR_NULL_PTR
+    assert call(lse=0) == ops.ATTN_ERR_NULL_PTR
+
+
+def test_misaligned_pointers():
+    for kw in (dict(q=Q + 8), dict(k=K + 2), dict(v=V + 4), dict(o=O + 1), dict(lse=L + 4)):
+        assert call(**kw) == ops.ATTN_ERR_MISALIGNED, kw
+
+
+def test_overlapping_outputs_are_rejected():
+    assert call(o=Q) == ops.ATTN_ERR_INVALID_ARG
+    assert call(lse=K + 64) == ops.ATTN_ERR_INVALID_ARG
+    assert call(o=V - 16) == ops.ATTN_ERR_INVALID_ARG
+
+
+def test_empty_work_returns_ok_without_launching():
+    # B == 0 or Sq == 0: nothing to compute, no CUDA call (passes on a machine without a GPU)
+    assert call(B=0) == ops.ATTN_OK
+    assert call(Sq=0) == ops.ATTN_OK
+    assert call(q=0, o=0, lse=0, Sq=0) == ops.ATTN_OK or call(q=0, o=0, lse=0, Sq=0) == ops.ATTN_ERR_NULL_PTR
+
+
+def test_keys_may_be_null_when_there_are_none():
+    # Sk == 0 needs no k/v: validation passes; without a GPU the device query then fails with a CUDA error
+    st = call(k=0, v=0, Sk=0)
+    assert st in (ops.ATTN_OK, ops.ATTN_ERR_CUDA, ops.ATTN_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_oracle_and_library_share_no_code():
+    # the oracle is plain C with no include of the library's headers, and the library never names the oracle
+    src = open(os.path.join(ROOT, "oracle", "attn_ref.c")).read()
+    assert "attn_fwd.h" not in src and "ptx.cuh" not in src
+    for f in os.listdir(os.path.join(ROOT, "attention_forward_06_gb300", "csrc")):
+        text = open(os.path.join(ROOT, "attention_forward_06_gb300", "csrc", f)).read()
+        assert "attn_ref" not in text and "oracle" not in text
+    for f in ("ops.py", "_lib.py", "build.py", "inputs.py", "__init__.py"):
+        text = open(os.path.join(ROOT, "attention_forward_06_gb300", f)).read()
+        assert "import oracle" not in text and "from oracle" not in text
+
+
+def test_nm_lists_c_symbols_unmangled(built):
+    out = subprocess.run(["nm", "-D", "--defined-only", built["attn_fwd"]], capture_output=True, text=True).stdout
+    for f in declared_functions(HEADERS["attn_fwd"]):
+        assert re.search(rf"\bT {f}$", out, flags=re.M), f

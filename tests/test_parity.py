@@ -1,0 +1,137 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, element by
+element on the same seeded inputs: small shapes that span several tiles and
+ragged tails, the edge cases (fully masked rows, one row, one key, no keys,
+grouped heads), and every benchmark workload at full size on sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_forward_06_gb300 import ops
+from attention_forward_06_gb300.inputs import WORKLOADS, bf16_bits, draw, draw_workload, sample_rows
+from parity_util import compare
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(q, k, v, causal, scale):
+    o, lse = ops.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    st, site = ops.debug_status()
+    assert st == ops.ATTN_OK, f"kernel wait ran out at site {site}"
+    return o.cpu(), lse.cpu()
+
+
+def full_check(B, Hq, Hkv, Sq, Sk, D, causal, seed, qk_std=1.0):
+    q, k, v = draw(B, Hq, Hkv, Sq, Sk, D, seed, qk_std=qk_std)
+    scale = float(np.float32(D ** -0.5))
+    o, lse = run_gpu(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal, scale)
+    return compare(o, lse, o_ref, lse_ref)
+
+
+SHAPES = [
+    # B, Hq, Hkv, Sq, Sk, D, causal
+    (1, 1, 1, 128, 128, 64, 0),       # one tile each
+    (1, 2, 2, 300, 300, 128, 1),      # two query blocks, ragged
+    (2, 4, 1, 129, 1000, 128, 0),     # ragged both ways, G = 4
+    (1, 8, 2, 1000, 129, 64, 1),      # Sq > Sk bottom-right: fully masked rows
+    (1, 2, 1, 1, 1, 128, 0),          # one row, one key
+    (1, 2, 1, 1, 257, 64, 1),         # one query row against three key tiles
+    (1, 1, 1, 257, 1, 128, 1),        # one key
+    (1, 4, 4, 127, 127, 64, 2),       # top-left, Sq = Sk
+    (1, 2, 1, 200, 700, 128, 2),      # top-left, Sq < Sk
+    (1, 2, 1, 700, 200, 64, 2),       # top-left, Sq > Sk
+    (1, 3, 3, 513, 513, 128, 1),      # three query blocks
+    (2, 8, 8, 256, 384, 64, 0),
+    (1, 8, 1, 256, 256, 128, 1),      # G = 8
+    (1, 2, 2, 100, 0, 128, 1),        # no keys at all
+    (1, 1, 1, 640, 1920, 128, 1),     # bottom-right, many tiles, ragged none
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes_match_oracle(shape):
+    B, Hq, Hkv, Sq, Sk, D, causal = shape
+    full_check(B, Hq, Hkv, Sq, Sk, D, causal, seed=sum(shape))
+
+
+def test_tiny_workload_matches_oracle():
+    w = WORKLOADS["tiny"]
+    stats = full_check(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.causal, w.seed)
+    assert stats["max_abs_dO"] <= 1e-2
+
+
+def test_sharp_logits_online_rescale():
+    # logits with standard deviation ~9 (Q, K entries N(0, 3^2)): the running max moves a lot
+    full_check(1, 4, 1, 512, 1536, 128, 1, seed=77, qk_std=3.0)
+    full_check(1, 2, 2, 384, 384, 64, 0, seed=78, qk_std=3.0)
+
+
+def test_train_workload_full_oracle():
+    w = WORKLOADS["train"]
+    full_check(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.causal, w.seed, w.qk_std)
+
+
+@pytest.mark.parametrize("name,per_head", [("gqa", 24), ("chunked128", 8), ("chunked64", 8), ("long", 12)])
+def test_full_size_workloads_on_sampled_rows(name, per_head):
+    w = WORKLOADS[name]
+    q, k, v = draw_workload(w)
+    o, lse = run_gpu(q, k, v, w.causal, w.scale)
+    rows = sample_rows(w.B, w.Hq, w.Sq, per_head, seed=w.seed + 1000)
+    o_ref, lse_ref = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), w.causal, w.scale, rows=rows)
+    o_rows = o.reshape(-1, w.D)[torch.from_numpy(rows)]
+    lse_rows = lse.reshape(-1)[torch.from_numpy(rows)]
+    compare(o_rows, lse_rows, o_ref, lse_ref)
+
+
+def test_deterministic_bitwise():
+    q, k, v = draw(2, 8, 2, 700, 900, 128, seed=5)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = ops.attn_fwd(qd, kd, vd, causal=1)
+    o2, l2 = ops.attn_fwd(qd, kd, vd, causal=1)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_gqa_equals_mha_with_repeated_heads():
+    q, k, v = draw(1, 8, 2, 384, 512, 128, seed=6)
+    G = 4
+    o1, l1 = run_gpu(q, k, v, 1, 0.088)
+    o2, l2 = run_gpu(q, k.repeat_interleave(G, 1), v.repeat_interleave(G, 1), 1, 0.088)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_chunked_equals_tail_of_full_causal():
+    Sq, Sk = 384, 1280
+    q, k, v = draw(1, 4, 2, Sk, Sk, 128, seed=8)
+    o_full, l_full = run_gpu(q, k, v, 1, 0.088)
+    o_c, l_c = run_gpu(q[:, :, Sk - Sq:].contiguous(), k, v, 1, 0.088)
+    assert torch.equal(o_c, o_full[:, :, Sk - Sq:]) and torch.equal(l_c, l_full[:, :, Sk - Sq:])
+
+
+def test_one_hot_rows_return_value_rows():
+    # q_i = 32 e0 and k_j* = 32 e0, all other keys 0: O_i = V[j*] exactly representable
+    Sq, Sk, D = 256, 640, 128
+    q = torch.zeros(1, 1, Sq, D); q[..., 0] = 32
+    k = torch.zeros(1, 1, Sk, D); k[0, 0, 333, 0] = 32
+    v = draw(1, 1, 1, 1, Sk, D, seed=9)[2]
+    o, lse = run_gpu(q.to(torch.bfloat16), k.to(torch.bfloat16), v, 0, float(np.float32(D ** -0.5)))
+    assert torch.equal(o[0, 0], v[0, 0, 333].expand(Sq, D))
+
+
+def test_outputs_written_through_given_buffers_and_stream():
+    q, k, v = [t.cuda() for t in draw(1, 2, 1, 200, 300, 64, seed=10)]
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((1, 2, 200), float("nan"), device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ops.attn_fwd(q, k, v, causal=0, o=o, lse=lse, stream=s)
+    s.synchronize()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+def test_wrong_dtype_is_rejected_by_binding():
+    q, k, v = [t.cuda() for t in draw(1, 1, 1, 16, 16, 64, seed=11)]
+    with pytest.raises(ValueError):
+        ops.attn_fwd(q.float(), k, v)
