@@ -21,7 +21,8 @@
 // m is only raised when a tile's max exceeds it by more than 8 (a factor 256);
 // otherwise the stale m stays, which is exact because O and the normaliser l
 // share it.  l sums the bf16-rounded P values the tensor cores multiply, so the
-// final O / l is a convex combination of V rows.  Causal masking touches only
+// final O / l is a convex combination of V rows; a second, fp32 sum of the
+// unrounded P gives the LSE.  Causal masking touches only
 // the tiles that straddle the diagonal (or the ragged end of K); tiles wholly
 // above the diagonal are never loaded.
 //
@@ -299,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float c = p.c;
     float m = -INFINITY;  // running max, log2 units
-    float l = 0.0f;       // running normaliser at max m
+    float l = 0.0f;       // sum of the bf16-rounded P the tensor cores use (normalises O)
+    float l_exact = 0.0f; // sum of the fp32 P (gives LSE)
     bool ok = true;
 
     for (int j = 0; j < n_tiles; ++j) {
@@ -329,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha = ex2_approx(m - m_tile);
         m = m_tile;
         l *= alpha;
+        l_exact *= alpha;
       }
       if (j > 0 && __any_sync(0xffffffffu, raise)) {
         // rescale this warp's 32 rows of O_t (PV_t(j-1) has completed: its commit preceded S_t(j)'s)
@@ -351,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p1 = ex2_approx(fmaf(s[half * 64 + 2 * i + 1], c, neg_m));
           pk[i] = pack_bf16x2(p0, p1);
           l += bf16lo_to_f32(pk[i]) + bf16hi_to_f32(pk[i]);
+          l_exact += p0 + p1;
         }
         tmem_st32(s_tmem + half * 32, pk);
       }
@@ -397,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0u, 0u, 0u, 0u);
     }
     if (live && (have_o || !aborted)) {
-      const float lse = any_key ? (m + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+      const float lse = any_key ? (m + lg2_approx(l_exact)) * 0.69314718055994531f : -INFINITY;
       p.lse[static_cast<int64_t>(bh) * p.Sq + row] = lse;
     }
   }
