@@ -4,13 +4,17 @@
 // on-chip softmax attention with a closed-form log-sum-exp normaliser).
 //
 // One CTA owns a work item: 256 query rows (two 128-row Q tiles) of one
-// (batch, query head).  Ten warps, each with one role:
+// (batch, query head).  Twelve warps:
 //   warps 0-3  softmax for Q tile 0 (one thread per query row)
 //   warps 4-7  softmax for Q tile 1
 //   warp  8    TMA producer: Q tiles once, then K/V tiles through a ring of
 //              shared-memory slots guarded by full/empty mbarriers
 //   warp  9    tcgen05 issuer: S_t = Q_t K^T into tensor memory (TMEM), and
 //              O_t += P_t V with P_t read back from TMEM; owns the TMEM allocation
+//   warps 10-11 idle (they complete the third warpgroup)
+// Registers are rebalanced per warpgroup after set-up: the softmax warpgroups
+// grow to 224 per thread (a whole S row lives in registers), the third shrinks
+// to 56; 128*56 + 256*224 equals the 384*168 the block is launched with.
 // The issuer interleaves the two Q tiles so the tensor cores work on one tile
 // while the other tile's softmax runs:
 //   S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
@@ -50,8 +54,12 @@ constexpr int BM = 128;          // query rows per Q tile (MMA M)
 constexpr int BN = 128;          // keys per K/V tile
 constexpr int QTILES = 2;        // Q tiles per work item
 constexpr int ROWS_PER_ITEM = QTILES * BM;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // 3 warpgroups
 constexpr int kLoadWarp = 8;
+constexpr uint32_t kRegsLaunch = 168;   // 65536 / 384, what ptxas assigns under the launch bounds
+constexpr uint32_t kRegsSoftmax = 224;  // warpgroups 0 and 1
+constexpr uint32_t kRegsOther = 56;     // warpgroup 2 (producer, issuer, two idle warps)
+static_assert(128 * kRegsOther + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split exceeds the pool");
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s per wait
@@ -159,6 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_slot;
   volatile uint32_t* abort_v = &abort_flag;
 
+  if (warp >= 8) {
+    regs_decrease<kRegsOther>();
+  }
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
     if (n_tiles > 0) {
@@ -283,8 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       warp_wait(&o_final, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax (+ rescale, epilogue)
+    regs_increase<kRegsSoftmax>();
     const int t = warp / 4;
     const int quarter = warp % 4;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -313,18 +325,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t r[128];
       tmem_ld128_wait(s_tmem, r);
-      float s[128];
-#pragma unroll
-      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
       if (j * BN + BN - 1 > lim_tile) {  // tile straddles the diagonal or the end of K
         const int kmax = lim - j * BN;
 #pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = (i > kmax) ? -INFINITY : s[i];
+        for (int i = 0; i < 128; ++i) r[i] = (i > kmax) ? __float_as_uint(-INFINITY) : r[i];
       }
-      float mx = s[0];
+      // row max: four independent chains of 3-input max
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
-      const float m_tile = mx * c;
+      for (int i = 0; i < 128; i += 8) {
+        mx0 = max3f(mx0, __uint_as_float(r[i + 0]), __uint_as_float(r[i + 1]));
+        mx1 = max3f(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+        mx2 = max3f(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+        mx3 = max3f(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+      }
+      const float m_tile = fmaxf(max3f(mx0, mx1, mx2), mx3) * c;
       const bool raise = m_tile > m + kRescaleThreshold;
       float alpha = 1.0f;
       if (raise) {
@@ -335,28 +350,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (j > 0 && __any_sync(0xffffffffu, raise)) {
         // rescale this warp's 32 rows of O_t (PV_t(j-1) has completed: its commit preceded S_t(j)'s)
+        const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
         for (int cb = 0; cb < D / 32; ++cb) {
           uint32_t o[32];
           tmem_ld32_wait(o_tmem + cb * 32, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            float x0, x1;
+            f2_unpack(fmul2(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), x0, x1);
+            o[i] = __float_as_uint(x0);
+            o[i + 1] = __float_as_uint(x1);
+          }
           tmem_st32(o_tmem + cb * 32, o);
         }
       }
+      // P = exp2(s * c - m): packed FMA, one ex2 per element, bf16 pairs; two sums
       const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+      const uint64_t c2 = f2_pack(c, c);
+      const uint64_t nm2 = f2_pack(neg_m, neg_m);
+      uint64_t le0 = f2_pack(0.0f, 0.0f), le1 = le0;
+      float lr0 = 0.0f, lr1 = 0.0f, lr2 = 0.0f, lr3 = 0.0f;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(fmaf(s[half * 64 + 2 * i], c, neg_m));
-          const float p1 = ex2_approx(fmaf(s[half * 64 + 2 * i + 1], c, neg_m));
+          const int e = half * 64 + 2 * i;
+          float x0, x1;
+          f2_unpack(ffma2(f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
           pk[i] = pack_bf16x2(p0, p1);
-          l += bf16lo_to_f32(pk[i]) + bf16hi_to_f32(pk[i]);
-          l_exact += p0 + p1;
+          if (i & 1) {
+            le1 = fadd2(le1, f2_pack(p0, p1));
+            add_bf16x2_to_f32(lr2, lr3, pk[i]);
+          } else {
+            le0 = fadd2(le0, f2_pack(p0, p1));
+            add_bf16x2_to_f32(lr0, lr1, pk[i]);
+          }
         }
         tmem_st32(s_tmem + half * 32, pk);
+      }
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(le0, a0, a1);
+        f2_unpack(le1, b0, b1);
+        l_exact += (a0 + a1) + (b0 + b1);
+        l += (lr0 + lr1) + (lr2 + lr3);
       }
       tmem_wait_st();
       tc_fence_before();
