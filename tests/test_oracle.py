@@ -44,6 +44,26 @@ def allowed_mask(Sq, Sk, causal):
 
 
 # ---------------------------------------------------------------- worked examples
+def closed_form_o(text):
+    from fractions import Fraction
+    return float(Fraction(text))
+
+
+def closed_form_lse(text):
+    """'-inf', '0', 'ln n' or 'k ln 2'."""
+    text = text.strip()
+    if text == "-inf":
+        return -math.inf
+    parts = text.split()
+    if parts == ["0"]:
+        return 0.0
+    if len(parts) == 2 and parts[0] == "ln":
+        return math.log(int(parts[1]))
+    if len(parts) == 3 and parts[1] == "ln":
+        return int(parts[0]) * math.log(int(parts[2]))
+    raise ValueError(text)
+
+
 def test_golden_closed_forms():
     spec = json.load(open(GOLDEN))
     scale, tol = spec["scale"], spec["tolerance"]
@@ -53,8 +73,8 @@ def test_golden_closed_forms():
         k = bits(case["k"])[None]
         v = bits(case["v"])[None]
         o, lse = oracle.attention(q, k, v, case["causal"], scale)
-        exp_o = np.array(case["o"], np.float64)[None]
-        exp_lse = np.array([[-np.inf if x is None else x for x in row] for row in case["lse"]])[None]
+        exp_o = np.vectorize(closed_form_o, otypes=[np.float64])(np.array(case["o"]))[None]
+        exp_lse = np.vectorize(closed_form_lse, otypes=[np.float64])(np.array(case["lse"]))[None]
         np.testing.assert_allclose(o, exp_o, rtol=0, atol=tol, err_msg=case["name"])
         finite = np.isfinite(exp_lse)
         np.testing.assert_allclose(lse[finite], exp_lse[finite], rtol=0, atol=tol, err_msg=case["name"])
