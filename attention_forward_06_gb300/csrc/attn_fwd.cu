@@ -3,32 +3,40 @@
 // Sparse Attention", technical summary section 1: FlashAttention's fused,
 // on-chip softmax attention with a closed-form log-sum-exp normaliser).
 //
-// One CTA owns a work item: 256 query rows (two 128-row Q tiles) of one
-// (batch, query head).  Twelve warps:
-//   warps 0-3  softmax for Q tile 0 (one thread per query row)
-//   warps 4-7  softmax for Q tile 1
-//   warp  8    TMA producer: Q tiles once, then K/V tiles through a ring of
-//              shared-memory slots guarded by full/empty mbarriers
-//   warp  9    tcgen05 issuer: S_t = Q_t K^T into tensor memory (TMEM), and
-//              O_t += P_t V with P_t read back from TMEM; owns the TMEM allocation
+// Persistent kernel: one CTA per SM walks a list of work items, each 256 query
+// rows (two 128-row Q tiles) of one (batch, query head).  Items are ordered
+// heaviest first (most key tiles under a causal mask) and dealt to the CTAs in
+// a boustrophedon order (0..G-1, then G-1..0, ...) so every CTA gets a similar
+// amount of work.  Twelve warps:
+//   warps 0-3   softmax for Q tile 0 (one thread per query row), then its epilogue
+//   warps 4-7   softmax for Q tile 1, then its epilogue
+//   warp  8     TMA producer: the Q tiles of an item, then its K/V tiles through a
+//               ring of shared-memory slots guarded by full/empty mbarriers
+//   warp  9     tcgen05 issuer: S_t = Q_t K^T into tensor memory (TMEM), and
+//               O_t += P_t V with P_t read back from TMEM; owns the TMEM allocation
 //   warps 10-11 idle (they complete the third warpgroup)
 // Registers are rebalanced per warpgroup after set-up: the softmax warpgroups
 // grow to 224 per thread (a whole S row lives in registers), the third shrinks
 // to 56; 128*56 + 256*224 equals the 384*168 the block is launched with.
+//
 // The issuer interleaves the two Q tiles so the tensor cores work on one tile
 // while the other tile's softmax runs:
 //   S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
+// and carries on into the next item while the softmax warps run the epilogue of
+// the last one: only the first P.V of the next item waits for the epilogue to
+// have read O out of TMEM (o_empty), and the next item's Q only waits for the
+// last S of this one (q_empty).
 // TMEM columns: S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [384,384+D); P_t
 // (bf16 pairs) overwrites the first 64 columns of S_t once S_t is in registers.
 //
 // Online softmax per row, in log2 units (c = scale * log2 e): the running max
 // m is only raised when a tile's max exceeds it by more than 8 (a factor 256);
-// otherwise the stale m stays, which is exact because O and the normaliser l
+// otherwise the stale m stays, which is exact because O and the normalisers
 // share it.  l sums the bf16-rounded P values the tensor cores multiply, so the
 // final O / l is a convex combination of V rows; a second, fp32 sum of the
-// unrounded P gives the LSE.  Causal masking touches only
-// the tiles that straddle the diagonal (or the ragged end of K); tiles wholly
-// above the diagonal are never loaded.
+// unrounded P gives the LSE.  Causal masking touches only the tiles that
+// straddle the diagonal (or the ragged end of K); tiles wholly above the
+// diagonal are never loaded.
 //
 // Every mbarrier wait is bounded: a wait that runs out sets a shared abort
 // flag and a device status word, and all roles unwind to the final barrier,
@@ -54,13 +62,13 @@ constexpr int BM = 128;          // query rows per Q tile (MMA M)
 constexpr int BN = 128;          // keys per K/V tile
 constexpr int QTILES = 2;        // Q tiles per work item
 constexpr int ROWS_PER_ITEM = QTILES * BM;
-constexpr int kThreads = 384;  // 3 warpgroups
+constexpr int kThreads = 384;    // 3 warpgroups
 constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kRegsLaunch = 168;   // 65536 / 384, what ptxas assigns under the launch bounds
 constexpr uint32_t kRegsSoftmax = 224;  // warpgroups 0 and 1
 constexpr uint32_t kRegsOther = 56;     // warpgroup 2 (producer, issuer, two idle warps)
 static_assert(128 * kRegsOther + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split exceeds the pool");
-constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s per wait
 constexpr uint64_t kDrainTimeoutNs = 500000000ull;
@@ -89,8 +97,42 @@ struct Params {
   int diag;
   int n_qblocks;  // ceil(Sq / ROWS_PER_ITEM)
   int BH;         // B * Hq
+  int n_items;    // BH * n_qblocks
   float c;        // scale * log2(e)
 };
+
+struct Item {
+  int bh;       // b * Hq + query head
+  int kv_z;     // b * Hkv + kv head
+  int q0;       // first query row
+  int n_tiles;  // key tiles to visit
+};
+
+// Item x of the heaviest-first list: query block from the last, heads fastest.
+__device__ __forceinline__ Item item_at(const Params& p, int x) {
+  Item it;
+  const int qb = p.n_qblocks - 1 - x / p.BH;
+  it.bh = x % p.BH;
+  const int b = it.bh / p.Hq;
+  const int hq = it.bh % p.Hq;
+  it.kv_z = b * p.Hkv + hq / p.G;
+  it.q0 = qb * ROWS_PER_ITEM;
+  int kv_end = p.Sk;
+  if (p.causal) {
+    const int last_row = min(it.q0 + ROWS_PER_ITEM, p.Sq) - 1;
+    kv_end = min(p.Sk, last_row + p.diag + 1);
+  }
+  it.n_tiles = kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
+  return it;
+}
+
+// k-th item of this CTA (boustrophedon deal), or -1 past the end.
+__device__ __forceinline__ int item_index(const Params& p, int k) {
+  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  const int x = k * G + ((k & 1) ? (G - 1 - c) : c);
+  return x < p.n_items ? x : -1;
+}
 
 __device__ int g_status;  // sticky: 0 = fine, else the site of the first wait that ran out
 
@@ -122,26 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* q_s = smem;               // Q tile t at q_s + t * kTileBytes
   uint8_t* kv_s = smem + C::kQBytes;  // slot s at kv_s + s * kTileBytes
   __shared__ uint64_t kv_full[S], kv_empty[S];
-  __shared__ uint64_t q_full, s_full[QTILES], p_full[QTILES], o_final;
+  __shared__ uint64_t q_full, q_empty, s_full[QTILES], p_full[QTILES], o_final, o_empty[QTILES], mma_drain;
   __shared__ uint32_t tmem_base_slot;
   __shared__ uint32_t abort_flag;
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-
-  // ---- work item: heaviest query blocks first (they have the most key tiles under a causal mask)
-  const int qb = p.n_qblocks - 1 - static_cast<int>(blockIdx.x) / p.BH;
-  const int bh = static_cast<int>(blockIdx.x) % p.BH;
-  const int b = bh / p.Hq;
-  const int hq = bh % p.Hq;
-  const int kv_z = b * p.Hkv + hq / p.G;
-  const int q0 = qb * ROWS_PER_ITEM;
-  int kv_end = p.Sk;
-  if (p.causal) {
-    const int last_row = min(q0 + ROWS_PER_ITEM, p.Sq) - 1;
-    kv_end = min(p.Sk, last_row + p.diag + 1);
-  }
-  const int n_tiles = kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -149,11 +177,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(&q_full, 1);
+    mbar_init(&q_empty, 1);
     for (int t = 0; t < QTILES; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 4 * 32);
+      mbar_init(&o_empty[t], 4 * 32);
     }
     mbar_init(&o_final, 1);
+    mbar_init(&mma_drain, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -168,104 +199,129 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* abort_v = &abort_flag;
 
   if (warp >= 8) {
-    regs_decrease<kRegsOther>();
-  }
-  if (warp == kLoadWarp) {
+   // warpgroup 2: every warp shrinks its registers at the same instruction, then splits by role
+   regs_decrease<kRegsOther>();
+   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (n_tiles > 0) {
+    if (lane == 0) {
+      tma_prefetch_map(&tq);
+      tma_prefetch_map(&tk);
+      tma_prefetch_map(&tv);
+    }
+    uint32_t kv_it = 0;     // K/V loads issued so far (over all items)
+    uint32_t q_issued = 0;  // Q loads issued so far (one per item with key tiles)
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int x = item_index(p, k);
+      if (x < 0) break;
+      const Item it = item_at(p, x);
+      if (it.n_tiles == 0) continue;
+      if (q_issued > 0) {  // the previous item's last S has finished reading Q
+        ok = warp_wait(&q_empty, (q_issued - 1) & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+      }
       if (lane == 0) {
-        tma_prefetch_map(&tq);
-        tma_prefetch_map(&tk);
-        tma_prefetch_map(&tv);
         mbar_arrive_expect_tx(&q_full, C::kQBytes);
         for (int t = 0; t < QTILES; ++t)
           for (int cb = 0; cb < D / 64; ++cb)
-            tma_load_3d(q_s + t * C::kTileBytes + cb * C::kColBlockBytes, &tq, &q_full, cb * 64, q0 + t * BM, bh);
+            tma_load_3d(q_s + t * C::kTileBytes + cb * C::kColBlockBytes, &tq, &q_full, cb * 64, it.q0 + t * BM,
+                        it.bh);
       }
       __syncwarp();
-      int issued = 0;  // K/V tile loads issued so far (K_j is load 2j, V_j is load 2j+1)
-      bool ok = true;
-      for (int it = 0; it < 2 * n_tiles && ok; ++it) {
-        const int slot = it % S;
-        const int use = it / S;
+      ++q_issued;
+      for (int i = 0; i < 2 * it.n_tiles; ++i) {  // K_j is load 2j, V_j is load 2j+1
+        const uint32_t slot = kv_it % S;
+        const uint32_t use = kv_it / S;
         if (use > 0) {
           ok = warp_wait(&kv_empty[slot], (use - 1) & 1, abort_v, kTimeoutNs);
-          if (!ok) {
-            if (lane == 0) record_abort(abort_v, kSiteProducer);
-            break;
-          }
+          if (!ok) break;
         }
         if (lane == 0) {
-          const int j = it >> 1;
-          const CUtensorMap* map = (it & 1) ? &tv : &tk;
+          const CUtensorMap* map = (i & 1) ? &tv : &tk;
           mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
           for (int cb = 0; cb < D / 64; ++cb)
             tma_load_3d(kv_s + slot * C::kTileBytes + cb * C::kColBlockBytes, map, &kv_full[slot], cb * 64,
-                        j * BN, kv_z);
+                        (i >> 1) * BN, it.kv_z);
         }
         __syncwarp();
-        ++issued;
+        ++kv_it;
       }
-      if (!ok || *abort_v) {
-        // unwinding: let the copies already in flight land before the CTA exits
-        mbar_wait_bounded(&q_full, 0, abort_v, kDrainTimeoutNs);
-        for (int it = (issued > S ? issued - S : 0); it < issued; ++it)
-          mbar_wait_bounded(&kv_full[it % S], (it / S) & 1, abort_v, kDrainTimeoutNs);
-      }
+    }
+    if (!ok) {
+      if (lane == 0) record_abort(abort_v, kSiteProducer);
+      // unwinding: let the copies already in flight land before the CTA exits
+      if (q_issued > 0) mbar_wait_bounded(&q_full, (q_issued - 1) & 1, abort_v, kDrainTimeoutNs);
+      for (uint32_t i = (kv_it > S ? kv_it - S : 0); i < kv_it; ++i)
+        mbar_wait_bounded(&kv_full[i % S], (i / S) & 1, abort_v, kDrainTimeoutNs);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tcgen05 issuer
-    if (n_tiles > 0) {
-      const uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
-      const uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
-      const uint32_t q_addr = smem_u32(q_s);
-      const uint32_t kv_addr = smem_u32(kv_s);
-      auto issue_s = [=](int t, int slot) {
-        const uint32_t qa = q_addr + t * C::kTileBytes;
-        const uint32_t ka = kv_addr + slot * C::kTileBytes;
+    const uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
+    const uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
+    const uint32_t q_addr = smem_u32(q_s);
+    const uint32_t kv_addr = smem_u32(kv_s);
+    // Operand descriptors are built once per tile; a K step moves the start
+    // address field (bits 0-13, address >> 4) by a constant, never carrying out.
+    auto issue_s = [=](int t, uint32_t slot) {
+      const uint32_t qlo = sdesc_sw128_lo(opaque(q_addr) + t * C::kTileBytes, 16);
+      const uint32_t klo = sdesc_sw128_lo(kv_addr + slot * C::kTileBytes, 16);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kColBlockBytes + (kk % 4) * 32;
-          mma_bf16_ss(tmem + t * BN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s,
-                      kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_pv = [=](int t, int slot, bool accumulate) {
-        const uint32_t va = kv_addr + slot * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ts(tmem + 2 * BN + t * 128, tmem + t * BN + kk * 8,
-                      sdesc_sw128(va + kk * 16 * 128, C::kColBlockBytes, 1024), idesc_pv,
-                      (accumulate || kk > 0) ? 1u : 0u);
-      };
-      bool ok = warp_wait(&q_full, 0, abort_v, kTimeoutNs);
-      int kslot = 0;
-      if (ok) ok = warp_wait(&kv_full[0], 0, abort_v, kTimeoutNs);
-      if (ok) {
-        tc_fence_after();
-        if (lane == 0) {
-          issue_s(0, kslot);
-          mma_commit(&s_full[0]);
-          issue_s(1, kslot);
-          mma_commit(&s_full[1]);
-          mma_commit(&kv_empty[kslot]);
-        }
-        __syncwarp();
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk / 4) * C::kColBlockBytes + (kk % 4) * 32) >> 4;
+        mma_bf16_ss_lo(tmem + t * BN, qlo + off, klo + off, sdesc_sw128_hi(1024), idesc_s, kk > 0 ? 1u : 0u);
       }
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int vit = 2 * j + 1;
-        const int vslot = vit % S;
-        ok = warp_wait(&kv_full[vslot], (vit / S) & 1, abort_v, kTimeoutNs);
-        if (ok) ok = warp_wait(&p_full[0], j & 1, abort_v, kTimeoutNs);
+    };
+    auto issue_pv = [=](int t, uint32_t slot, bool accumulate) {
+      const uint32_t vlo = sdesc_sw128_lo(opaque(kv_addr) + slot * C::kTileBytes, C::kColBlockBytes);
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk)
+        mma_bf16_ts_lo(tmem + 2 * BN + t * 128, tmem + t * BN + kk * 8, vlo + ((kk * 16 * 128) >> 4),
+                       sdesc_sw128_hi(1024), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+    };
+    // wait for load number `n` of the K/V stream
+    auto wait_kv = [&](uint32_t n) {
+      return warp_wait(&kv_full[n % S], (n / S) & 1, abort_v, kTimeoutNs);
+    };
+    uint32_t kv_it = 0;   // K/V loads consumed
+    uint32_t g = 0;       // key tiles processed over all items (p_full phase)
+    uint32_t n_done = 0;  // items with key tiles processed
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int x = item_index(p, k);
+      if (x < 0) break;
+      const Item it = item_at(p, x);
+      const int n = it.n_tiles;
+      if (n == 0) continue;
+      ok = warp_wait(&q_full, n_done & 1, abort_v, kTimeoutNs);
+      if (ok) ok = wait_kv(kv_it);
+      if (!ok) break;
+      uint32_t kslot = kv_it % S;
+      ++kv_it;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(0, kslot);
+        mma_commit(&s_full[0]);
+        issue_s(1, kslot);
+        mma_commit(&s_full[1]);
+        mma_commit(&kv_empty[kslot]);
+        if (n == 1) mma_commit(&q_empty);
+      }
+      __syncwarp();
+      for (int j = 0; j < n; ++j) {
+        const uint32_t vslot = kv_it % S;
+        ok = wait_kv(kv_it);
+        ++kv_it;
+        if (ok && j == 0 && n_done > 0) ok = warp_wait(&o_empty[0], (n_done - 1) & 1, abort_v, kTimeoutNs);
+        if (ok) ok = warp_wait(&p_full[0], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) issue_pv(0, vslot, j > 0);
         __syncwarp();
-        const bool more = j + 1 < n_tiles;
+        const bool more = j + 1 < n;
         if (more) {
-          const int kit = 2 * j + 2;
-          kslot = kit % S;
-          ok = warp_wait(&kv_full[kslot], (kit / S) & 1, abort_v, kTimeoutNs);
+          kslot = kv_it % S;
+          ok = wait_kv(kv_it);
+          ++kv_it;
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
@@ -274,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
-        ok = warp_wait(&p_full[1], j & 1, abort_v, kTimeoutNs);
+        if (j == 0 && n_done > 0) ok = warp_wait(&o_empty[1], (n_done - 1) & 1, abort_v, kTimeoutNs);
+        if (ok) ok = warp_wait(&p_full[1], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -284,17 +341,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_s(1, kslot);
             mma_commit(&s_full[1]);
             mma_commit(&kv_empty[kslot]);
+            if (j + 2 == n) mma_commit(&q_empty);  // that was the item's last S
           }
         }
         __syncwarp();
+        ++g;
       }
-      if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
-      // o_final: every MMA issued above has completed (also the drain before TMEM is freed)
+      if (!ok) break;
       if (lane == 0) mma_commit(&o_final);
       __syncwarp();
-      warp_wait(&o_final, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
+      ++n_done;
     }
-  } else if (warp < 8) {
+    if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
+    // every MMA issued above has completed before TMEM can be freed
+    if (lane == 0) mma_commit(&mma_drain);
+    __syncwarp();
+    warp_wait(&mma_drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
+   }
+  } else {
     // ------------------------------------------------------------ softmax (+ rescale, epilogue)
     regs_increase<kRegsSoftmax>();
     const int t = warp / 4;
@@ -302,148 +366,170 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + t * BN;
     const uint32_t o_tmem = tmem + lane_off + 2 * BN + t * 128;
-    const int row = q0 + t * BM + quarter * 32 + lane;  // global query row
-    const int tile_row0 = q0 + t * BM;
-    // last allowed key of this row, and of the tile's first row (the most restricted)
-    int lim = p.Sk - 1, lim_tile = p.Sk - 1;
-    if (p.causal) {
-      lim = min(lim, row + p.diag);
-      lim_tile = min(lim_tile, tile_row0 + p.diag);
-    }
     const float c = p.c;
-    float m = -INFINITY;  // running max, log2 units
-    float l = 0.0f;       // sum of the bf16-rounded P the tensor cores use (normalises O)
-    float l_exact = 0.0f; // sum of the fp32 P (gives LSE)
+    uint32_t g = 0;       // key tiles processed over all items (s_full phase)
+    uint32_t n_done = 0;  // items with key tiles processed (o_final phase)
     bool ok = true;
 
-    for (int j = 0; j < n_tiles; ++j) {
-      ok = warp_wait(&s_full[t], j & 1, abort_v, kTimeoutNs);
+    for (int k = 0; ok; ++k) {
+      const int x = item_index(p, k);
+      if (x < 0) break;
+      const Item it = item_at(p, x);
+      const int row = it.q0 + t * BM + quarter * 32 + lane;  // global query row
+      const bool live = row < p.Sq;
+      __nv_bfloat16* orow = p.o + (static_cast<int64_t>(it.bh) * p.Sq + row) * D;
+      float* lrow = p.lse + static_cast<int64_t>(it.bh) * p.Sq + row;
+      if (it.n_tiles == 0) {  // no key is visible to any row of this item
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0u, 0u, 0u, 0u);
+          *lrow = -INFINITY;
+        }
+        continue;
+      }
+      // last allowed key of this row, and of the tile's first row (the most restricted)
+      const int tile_row0 = it.q0 + t * BM;
+      int lim = p.Sk - 1, lim_tile = p.Sk - 1;
+      if (p.causal) {
+        lim = min(lim, row + p.diag);
+        lim_tile = min(lim_tile, tile_row0 + p.diag);
+      }
+      float m = -INFINITY;   // running max, log2 units
+      float l = 0.0f;        // sum of the bf16-rounded P the tensor cores use (normalises O)
+      float l_exact = 0.0f;  // sum of the fp32 P (gives LSE)
+
+      for (int j = 0; j < it.n_tiles; ++j, ++g) {
+        ok = warp_wait(&s_full[t], g & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r[128];
+        tmem_ld128_wait(s_tmem, r);
+        if (j * BN + BN - 1 > lim_tile) {  // tile straddles the diagonal or the end of K
+          const int kmax = lim - j * BN;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) r[i] = (i > kmax) ? __float_as_uint(-INFINITY) : r[i];
+        }
+        // row max: four independent chains of 3-input max
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 128; i += 8) {
+          mx0 = max3f(mx0, __uint_as_float(r[i + 0]), __uint_as_float(r[i + 1]));
+          mx1 = max3f(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+          mx2 = max3f(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+          mx3 = max3f(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+        }
+        const float m_tile = fmaxf(max3f(mx0, mx1, mx2), mx3) * c;
+        const bool raise = m_tile > m + kRescaleThreshold;
+        float alpha = 1.0f;
+        if (raise) {
+          alpha = ex2_approx(m - m_tile);
+          m = m_tile;
+          l *= alpha;
+          l_exact *= alpha;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+          // rescale this warp's 32 rows of O_t (PV_t(j-1) has completed: its commit preceded S_t(j)'s)
+          const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+          for (int cb = 0; cb < D / 32; ++cb) {
+            uint32_t o[32];
+            tmem_ld32_wait(o_tmem + cb * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float x0, x1;
+              f2_unpack(fmul2(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), x0, x1);
+              o[i] = __float_as_uint(x0);
+              o[i + 1] = __float_as_uint(x1);
+            }
+            tmem_st32(o_tmem + cb * 32, o);
+          }
+        }
+        // P = exp2(s * c - m): packed FMA, one ex2 per element, bf16 pairs; two sums
+        const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+        const uint64_t c2 = f2_pack(c, c);
+        const uint64_t nm2 = f2_pack(neg_m, neg_m);
+        uint64_t le0 = f2_pack(0.0f, 0.0f), le1 = le0;
+        float lr0 = 0.0f, lr1 = 0.0f, lr2 = 0.0f, lr3 = 0.0f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int e = half * 64 + 2 * i;
+            float x0, x1;
+            f2_unpack(ffma2(f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2), x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            pk[i] = pack_bf16x2(p0, p1);
+            if (i & 1) {
+              le1 = fadd2(le1, f2_pack(p0, p1));
+              add_bf16x2_to_f32(lr2, lr3, pk[i]);
+            } else {
+              le0 = fadd2(le0, f2_pack(p0, p1));
+              add_bf16x2_to_f32(lr0, lr1, pk[i]);
+            }
+          }
+          tmem_st32(s_tmem + half * 32, pk);
+        }
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(le0, a0, a1);
+          f2_unpack(le1, b0, b1);
+          l_exact += (a0 + a1) + (b0 + b1);
+          l += (lr0 + lr1) + (lr2 + lr3);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[t]);
+      }
       if (!ok) {
         if (lane == 0) record_abort(abort_v, kSiteSoftmax);
         break;
       }
+
+      // ---- epilogue: O = O_acc / l in bf16, LSE = (m + log2 l_exact) * ln 2
+      ok = warp_wait(&o_final, n_done & 1, abort_v, kTimeoutNs);
+      if (!ok) {
+        if (lane == 0) record_abort(abort_v, kSiteEpilogue);
+        break;
+      }
+      ++n_done;
       tc_fence_after();
-      uint32_t r[128];
-      tmem_ld128_wait(s_tmem, r);
-      if (j * BN + BN - 1 > lim_tile) {  // tile straddles the diagonal or the end of K
-        const int kmax = lim - j * BN;
-#pragma unroll
-        for (int i = 0; i < 128; ++i) r[i] = (i > kmax) ? __float_as_uint(-INFINITY) : r[i];
-      }
-      // row max: four independent chains of 3-input max
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 128; i += 8) {
-        mx0 = max3f(mx0, __uint_as_float(r[i + 0]), __uint_as_float(r[i + 1]));
-        mx1 = max3f(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-        mx2 = max3f(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
-        mx3 = max3f(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
-      }
-      const float m_tile = fmaxf(max3f(mx0, mx1, mx2), mx3) * c;
-      const bool raise = m_tile > m + kRescaleThreshold;
-      float alpha = 1.0f;
-      if (raise) {
-        alpha = ex2_approx(m - m_tile);
-        m = m_tile;
-        l *= alpha;
-        l_exact *= alpha;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, raise)) {
-        // rescale this warp's 32 rows of O_t (PV_t(j-1) has completed: its commit preceded S_t(j)'s)
-        const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          uint32_t o[32];
-          tmem_ld32_wait(o_tmem + cb * 32, o);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float x0, x1;
-            f2_unpack(fmul2(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), x0, x1);
-            o[i] = __float_as_uint(x0);
-            o[i + 1] = __float_as_uint(x1);
-          }
-          tmem_st32(o_tmem + cb * 32, o);
-        }
-      }
-      // P = exp2(s * c - m): packed FMA, one ex2 per element, bf16 pairs; two sums
-      const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-      const uint64_t c2 = f2_pack(c, c);
-      const uint64_t nm2 = f2_pack(neg_m, neg_m);
-      uint64_t le0 = f2_pack(0.0f, 0.0f), le1 = le0;
-      float lr0 = 0.0f, lr1 = 0.0f, lr2 = 0.0f, lr3 = 0.0f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+      uint32_t o[D];
+      if constexpr (D == 128) {
+        tmem_ld128_wait(o_tmem, o);
+      } else {
+        uint32_t lo[32], hi[32];
+        tmem_ld32_wait(o_tmem, lo);
+        tmem_ld32_wait(o_tmem + 32, hi);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int e = half * 64 + 2 * i;
-          float x0, x1;
-          f2_unpack(ffma2(f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2), x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          pk[i] = pack_bf16x2(p0, p1);
-          if (i & 1) {
-            le1 = fadd2(le1, f2_pack(p0, p1));
-            add_bf16x2_to_f32(lr2, lr3, pk[i]);
-          } else {
-            le0 = fadd2(le0, f2_pack(p0, p1));
-            add_bf16x2_to_f32(lr0, lr1, pk[i]);
-          }
+          o[i] = lo[i];
+          o[32 + i] = hi[i];
         }
-        tmem_st32(s_tmem + half * 32, pk);
       }
-      {
-        float a0, a1, b0, b1;
-        f2_unpack(le0, a0, a1);
-        f2_unpack(le1, b0, b1);
-        l_exact += (a0 + a1) + (b0 + b1);
-        l += (lr0 + lr1) + (lr2 + lr3);
-      }
-      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[t]);
-    }
-
-    // ---- epilogue: O = O_acc / l in bf16, LSE = (m + log2 l) * ln 2
-    bool have_o = false;
-    const bool aborted = __any_sync(0xffffffffu, *abort_v != 0);  // warp-uniform view of the flag
-    if (n_tiles > 0 && ok && !aborted) {
-      have_o = warp_wait(&o_final, 0, abort_v, kTimeoutNs);
-      if (!have_o) {
-        if (lane == 0) record_abort(abort_v, kSiteEpilogue);
-      } else {
-        tc_fence_after();
-      }
-    }
-    const bool live = row < p.Sq;
-    const bool any_key = have_o && l > 0.0f;
-    const float inv_l = any_key ? 1.0f / l : 0.0f;
-    __nv_bfloat16* orow = p.o + (static_cast<int64_t>(bh) * p.Sq + row) * D;
-    if (have_o) {
-      __syncwarp();
+      mbar_arrive(&o_empty[t]);  // O_t may now be overwritten by the next item's first P.V
+      const bool any_key = l > 0.0f;
+      const float inv_l = any_key ? 1.0f / l : 0.0f;
+      if (live) {
+        const uint64_t s2 = f2_pack(inv_l, inv_l);
+        uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-      for (int cb = 0; cb < D / 32; ++cb) {
-        uint32_t o[32];
-        tmem_ld32_wait(o_tmem + cb * 32, o);
-        uint32_t pk[16];
+        for (int v4 = 0; v4 < D / 8; ++v4) {
+          uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          for (int h = 0; h < 4; ++h) {
+            float x0, x1;
+            const int e = v4 * 8 + 2 * h;
+            f2_unpack(fmul2(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), s2), x0, x1);
+            w[h] = pack_bf16x2(x0, x1);
+          }
+          dst[v4] = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        *lrow = any_key ? (m + lg2_approx(l_exact)) * 0.69314718055994531f : -INFINITY;
       }
-    } else if (live && !aborted) {
-      uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-      for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    if (live && (have_o || !aborted)) {
-      const float lse = any_key ? (m + lg2_approx(l_exact)) * 0.69314718055994531f : -INFINITY;
-      p.lse[static_cast<int64_t>(bh) * p.Sq + row] = lse;
     }
   }
 
@@ -468,6 +554,7 @@ int cuda_fail(cudaError_t e) {
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mutex;
 int g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 unsupported
+int g_dev_sms[kMaxDevices];    // streaming multiprocessors per device
 
 // Capability check and kernel attributes, once per device.
 int prepare_device(int dev) {
@@ -483,6 +570,10 @@ int prepare_device(int dev) {
     g_dev_state[dev] = -1;
     return ATTN_ERR_UNSUPPORTED_DEVICE;
   }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_dev_sms[dev] = sms;
   e = cudaFuncSetAttribute(attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<128>::kSmemBytes);
   if (e == cudaSuccess)
@@ -570,8 +661,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   prm.diag = causal == 1 ? Sk - Sq : 0;
   prm.n_qblocks = static_cast<int>(n_qblocks);
   prm.BH = B * Hq;
+  prm.n_items = static_cast<int>(grid64);
   prm.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-  const int grid = static_cast<int>(grid64);
+  // persistent: one CTA per SM (shared memory and TMEM allow no second), never more CTAs than items
+  const int grid = static_cast<int>(grid64 < g_dev_sms[dev] ? grid64 : g_dev_sms[dev]);
   return D == 128 ? launch<128>(tq, tk, tv, prm, grid, stream) : launch<64>(tq, tk, tv, prm, grid, stream);
 }
 
