@@ -260,23 +260,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
     const uint32_t q_addr = smem_u32(q_s);
     const uint32_t kv_addr = smem_u32(kv_s);
+    // The whole warp runs the issue code (converged); one elected lane issues.
     // Operand descriptors are built once per tile; a K step moves the start
     // address field (bits 0-13, address >> 4) by a constant, never carrying out.
     auto issue_s = [=](int t, uint32_t slot) {
-      const uint32_t qlo = sdesc_sw128_lo(opaque(q_addr) + t * C::kTileBytes, 16);
-      const uint32_t klo = sdesc_sw128_lo(kv_addr + slot * C::kTileBytes, 16);
+      const uint64_t qd = sdesc_sw128(opaque(q_addr) + t * C::kTileBytes, 16, 1024);
+      const uint64_t kd = sdesc_sw128(kv_addr + slot * C::kTileBytes, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk / 4) * C::kColBlockBytes + (kk % 4) * 32) >> 4;
-        mma_bf16_ss_lo(tmem + t * BN, qlo + off, klo + off, sdesc_sw128_hi(1024), idesc_s, kk > 0 ? 1u : 0u);
+        mma_bf16_ss_elect(tmem + t * BN, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
     };
     auto issue_pv = [=](int t, uint32_t slot, bool accumulate) {
-      const uint32_t vlo = sdesc_sw128_lo(opaque(kv_addr) + slot * C::kTileBytes, C::kColBlockBytes);
+      const uint64_t vd = sdesc_sw128(opaque(kv_addr) + slot * C::kTileBytes, C::kColBlockBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk)
-        mma_bf16_ts_lo(tmem + 2 * BN + t * 128, tmem + t * BN + kk * 8, vlo + ((kk * 16 * 128) >> 4),
-                       sdesc_sw128_hi(1024), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+        mma_bf16_ts_elect(tmem + 2 * BN + t * 128, tmem + t * BN + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
+                          (accumulate || kk > 0) ? 1u : 0u);
     };
     // wait for load number `n` of the K/V stream
     auto wait_kv = [&](uint32_t n) {
@@ -298,15 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kslot = kv_it % S;
       ++kv_it;
       tc_fence_after();
-      if (lane == 0) {
-        issue_s(0, kslot);
-        mma_commit(&s_full[0]);
-        issue_s(1, kslot);
-        mma_commit(&s_full[1]);
-        mma_commit(&kv_empty[kslot]);
-        if (n == 1) mma_commit(&q_empty);
-      }
-      __syncwarp();
+      issue_s(0, kslot);
+      mma_commit_elect(&s_full[0]);
+      issue_s(1, kslot);
+      mma_commit_elect(&s_full[1]);
+      mma_commit_elect(&kv_empty[kslot]);
+      if (n == 1) mma_commit_elect(&q_empty);
       for (int j = 0; j < n; ++j) {
         const uint32_t vslot = kv_it % S;
         ok = wait_kv(kv_it);
@@ -315,8 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = warp_wait(&p_full[0], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) issue_pv(0, vslot, j > 0);
-        __syncwarp();
+        issue_pv(0, vslot, j > 0);
         const bool more = j + 1 < n;
         if (more) {
           kslot = kv_it % S;
@@ -324,38 +321,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++kv_it;
           if (!ok) break;
           tc_fence_after();
-          if (lane == 0) {
-            issue_s(0, kslot);
-            mma_commit(&s_full[0]);
-          }
-          __syncwarp();
+          issue_s(0, kslot);
+          mma_commit_elect(&s_full[0]);
         }
         if (j == 0 && n_done > 0) ok = warp_wait(&o_empty[1], (n_done - 1) & 1, abort_v, kTimeoutNs);
         if (ok) ok = warp_wait(&p_full[1], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
-          issue_pv(1, vslot, j > 0);
-          mma_commit(&kv_empty[vslot]);
-          if (more) {
-            issue_s(1, kslot);
-            mma_commit(&s_full[1]);
-            mma_commit(&kv_empty[kslot]);
-            if (j + 2 == n) mma_commit(&q_empty);  // that was the item's last S
-          }
+        issue_pv(1, vslot, j > 0);
+        mma_commit_elect(&kv_empty[vslot]);
+        if (more) {
+          issue_s(1, kslot);
+          mma_commit_elect(&s_full[1]);
+          mma_commit_elect(&kv_empty[kslot]);
+          if (j + 2 == n) mma_commit_elect(&q_empty);  // that was the item's last S
         }
-        __syncwarp();
         ++g;
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(&o_final);
-      __syncwarp();
+      mma_commit_elect(&o_final);
       ++n_done;
     }
     if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
     // every MMA issued above has completed before TMEM can be freed
-    if (lane == 0) mma_commit(&mma_drain);
-    __syncwarp();
+    mma_commit_elect(&mma_drain);
     warp_wait(&mma_drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
    }
   } else {
