@@ -220,14 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = warp_wait(&q_empty, (q_issued - 1) & 1, abort_v, kTimeoutNs);
         if (!ok) break;
       }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&q_full, C::kQBytes);
-        for (int t = 0; t < QTILES; ++t)
-          for (int cb = 0; cb < D / 64; ++cb)
-            tma_load_3d(q_s + t * C::kTileBytes + cb * C::kColBlockBytes, &tq, &q_full, cb * 64, it.q0 + t * BM,
-                        it.bh);
-      }
-      __syncwarp();
+      mbar_arrive_expect_tx_elect(&q_full, C::kQBytes);
+#pragma unroll
+      for (int t = 0; t < QTILES; ++t)
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb)
+          tma_load_3d_elect(q_s + t * C::kTileBytes + cb * C::kColBlockBytes, &tq, &q_full, cb * 64, it.q0 + t * BM,
+                            it.bh);
       ++q_issued;
       for (int i = 0; i < 2 * it.n_tiles; ++i) {  // K_j is load 2j, V_j is load 2j+1
         const uint32_t slot = kv_it % S;
@@ -236,14 +235,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = warp_wait(&kv_empty[slot], (use - 1) & 1, abort_v, kTimeoutNs);
           if (!ok) break;
         }
-        if (lane == 0) {
-          const CUtensorMap* map = (i & 1) ? &tv : &tk;
-          mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
-          for (int cb = 0; cb < D / 64; ++cb)
-            tma_load_3d(kv_s + slot * C::kTileBytes + cb * C::kColBlockBytes, map, &kv_full[slot], cb * 64,
-                        (i >> 1) * BN, it.kv_z);
-        }
-        __syncwarp();
+        const CUtensorMap* map = (i & 1) ? &tv : &tk;
+        mbar_arrive_expect_tx_elect(&kv_full[slot], C::kTileBytes);
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb)
+          tma_load_3d_elect(kv_s + slot * C::kTileBytes + cb * C::kColBlockBytes, map, &kv_full[slot], cb * 64,
+                            (i >> 1) * BN, it.kv_z);
         ++kv_it;
       }
     }
