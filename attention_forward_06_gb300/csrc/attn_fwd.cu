@@ -84,9 +84,13 @@ template <int D>
 struct Cfg {
   static constexpr int kTileBytes = BN * D * 2;            // one K or V tile; also one Q tile
   static constexpr int kColBlockBytes = BN * 128;          // 64 columns x 128 rows, 128-B swizzled
-  static constexpr int kStages = (D == 128) ? 5 : 8;       // K/V ring slots
+  static constexpr int kStages = (D == 128) ? 4 : 8;       // K/V ring slots
   static constexpr int kQBytes = QTILES * BM * D * 2;
-  static constexpr int kSmemBytes = kQBytes + kStages * kTileBytes + 1024;  // + alignment slack
+  static constexpr int kStageBytes = BM * D * 2;           // one Q tile of O in bf16, 128-B swizzled
+  static constexpr int kStageBufs = (D == 128) ? 1 : 2;    // O staging buffers (1: the two Q tiles take turns)
+  static constexpr int kSmemBytes =
+      kQBytes + kStages * kTileBytes + kStageBufs * kStageBytes + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 struct Params {
@@ -156,15 +160,18 @@ __device__ __forceinline__ void record_abort(volatile uint32_t* abort_flag, int 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, const Params p) {
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                    const Params p) {
   using C = Cfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint8_t* q_s = smem;               // Q tile t at q_s + t * kTileBytes
   uint8_t* kv_s = smem + C::kQBytes;  // slot s at kv_s + s * kTileBytes
+  uint8_t* st_s = kv_s + S * C::kTileBytes;  // O staging buffer b at st_s + b * kStageBytes
   __shared__ uint64_t kv_full[S], kv_empty[S];
-  __shared__ uint64_t q_full, q_empty, s_full[QTILES], p_full[QTILES], o_final, o_empty[QTILES], mma_drain;
+  __shared__ uint64_t q_full, q_empty, s_full[QTILES], p_full[QTILES], o_final[QTILES], o_empty[QTILES];
+  __shared__ uint64_t stage_rel[QTILES], mma_drain;
   __shared__ uint32_t tmem_base_slot;
   __shared__ uint32_t abort_flag;
 
@@ -182,8 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 4 * 32);
       mbar_init(&o_empty[t], 4 * 32);
+      mbar_init(&o_final[t], 1);
+      mbar_init(&stage_rel[t], 1);
     }
-    mbar_init(&o_final, 1);
     mbar_init(&mma_drain, 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -311,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         issue_pv(0, vslot, j > 0);
+        if (j + 1 == n) mma_commit_elect(&o_final[0]);  // O_0 complete: its epilogue can start
         const bool more = j + 1 < n;
         if (more) {
           kslot = kv_it % S;
@@ -326,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         issue_pv(1, vslot, j > 0);
+        if (j + 1 == n) mma_commit_elect(&o_final[1]);
         mma_commit_elect(&kv_empty[vslot]);
         if (more) {
           issue_s(1, kslot);
@@ -336,7 +346,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++g;
       }
       if (!ok) break;
-      mma_commit_elect(&o_final);
       ++n_done;
     }
     if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
@@ -354,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_tmem = tmem + lane_off + 2 * BN + t * 128;
     const float c = p.c;
     uint32_t g = 0;       // key tiles processed over all items (s_full phase)
-    uint32_t n_done = 0;  // items with key tiles processed (o_final phase)
+    uint32_t n_done = 0;  // items with key tiles processed (o_final[t] and staging phase)
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
@@ -474,13 +483,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
 
-      // ---- epilogue: O = O_acc / l in bf16, LSE = (m + log2 l_exact) * ln 2
-      ok = warp_wait(&o_final, n_done & 1, abort_v, kTimeoutNs);
+      // ---- epilogue: O = O_acc / l in bf16, LSE = (m + log2 l_exact) * ln 2.  O goes
+      // through a 128-B-swizzled staging tile in shared memory and out with one TMA
+      // store per 64 columns (coalesced; rows past Sq are clipped by the tensor map).
+      ok = warp_wait(&o_final[t], n_done & 1, abort_v, kTimeoutNs);
       if (!ok) {
         if (lane == 0) record_abort(abort_v, kSiteEpilogue);
         break;
       }
-      ++n_done;
+      const uint32_t e_idx = n_done++;  // this Q tile's epilogue count (staging hand-off phase)
       tc_fence_after();
       uint32_t o[D];
       if constexpr (D == 128) {
@@ -499,24 +510,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&o_empty[t]);  // O_t may now be overwritten by the next item's first P.V
       const bool any_key = l > 0.0f;
       const float inv_l = any_key ? 1.0f / l : 0.0f;
-      if (live) {
+      // the staging buffer: with one buffer the Q tiles take turns (tile 0, then tile 1, per item)
+      const int sb = (C::kStageBufs == 1) ? 0 : t;
+      uint8_t* stage = st_s + sb * C::kStageBytes;
+      if (C::kStageBufs == 1) {
+        if (t == 0) {
+          if (e_idx > 0) ok = warp_wait(&stage_rel[1], (e_idx - 1) & 1, abort_v, kTimeoutNs);
+        } else {
+          ok = warp_wait(&stage_rel[0], e_idx & 1, abort_v, kTimeoutNs);
+        }
+      } else if (e_idx > 0) {
+        ok = warp_wait(&stage_rel[t], (e_idx - 1) & 1, abort_v, kTimeoutNs);
+      }
+      if (!ok) {
+        if (lane == 0) record_abort(abort_v, kSiteEpilogue);
+        break;
+      }
+      {
+        const int r = quarter * 32 + lane;  // row within the Q tile
         const uint64_t s2 = f2_pack(inv_l, inv_l);
-        uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-        for (int v4 = 0; v4 < D / 8; ++v4) {
+        for (int ch = 0; ch < D / 8; ++ch) {  // 16-byte chunks of the row
           uint32_t w[4];
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             float x0, x1;
-            const int e = v4 * 8 + 2 * h;
+            const int e = ch * 8 + 2 * h;
             f2_unpack(fmul2(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), s2), x0, x1);
             w[h] = pack_bf16x2(x0, x1);
           }
-          dst[v4] = make_uint4(w[0], w[1], w[2], w[3]);
+          const int cb = ch / 8, cc = ch % 8;
+          uint4* dst = reinterpret_cast<uint4*>(stage + cb * (BM * 128) + r * 128 + ((cc ^ (r & 7)) << 4));
+          *dst = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        *lrow = any_key ? (m + lg2_approx(l_exact)) * 0.69314718055994531f : -INFINITY;
       }
+      fence_proxy_async_smem();
+      named_barrier_sync(1 + t, 128);  // the whole tile is staged
+      if (quarter == 0) {
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb)
+          tma_store_3d_elect(&to, stage + cb * (BM * 128), cb * 64, it.q0 + t * BM, it.bh);
+        bulk_commit_group_elect();
+        bulk_wait_group_read0();  // the staging tile has been read: hand it on
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&stage_rel[t]);
+      }
+      if (live) *lrow = any_key ? (m + lg2_approx(l_exact)) * 0.69314718055994531f : -INFINITY;
     }
+    if (quarter == 0) bulk_wait_group0();  // this warp's TMA stores have landed
   }
 
   tc_fence_before();
@@ -578,9 +619,9 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 template <int D>
-int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const Params& prm, int grid,
-           cudaStream_t stream) {
-  attn_fwd_kernel<D><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, prm);
+int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+           const Params& prm, int grid, cudaStream_t stream) {
+  attn_fwd_kernel<D><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -625,8 +666,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (st != ATTN_OK) return st;
 
   // ---- TMA maps: Q [B*Hq][Sq][D], K/V [B*Hkv][Sk][D]; boxes of 64 columns x 128 rows
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!attn_host::encode_bf16_rows(&tq, q, D, Sq, static_cast<uint64_t>(B) * Hq, BM)) return ATTN_ERR_TENSOR_MAP;
+  if (!attn_host::encode_bf16_rows(&to, o, D, Sq, static_cast<uint64_t>(B) * Hq, BM)) return ATTN_ERR_TENSOR_MAP;
   if (Sk > 0) {
     if (!attn_host::encode_bf16_rows(&tk, k, D, Sk, static_cast<uint64_t>(B) * Hkv, BN)) return ATTN_ERR_TENSOR_MAP;
     if (!attn_host::encode_bf16_rows(&tv, v, D, Sk, static_cast<uint64_t>(B) * Hkv, BN)) return ATTN_ERR_TENSOR_MAP;
@@ -651,7 +693,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   prm.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   // persistent: one CTA per SM (shared memory and TMEM allow no second), never more CTAs than items
   const int grid = static_cast<int>(grid64 < g_dev_sms[dev] ? grid64 : g_dev_sms[dev]);
-  return D == 128 ? launch<128>(tq, tk, tv, prm, grid, stream) : launch<64>(tq, tk, tv, prm, grid, stream);
+  return D == 128 ? launch<128>(tq, tk, tv, to, prm, grid, stream) : launch<64>(tq, tk, tv, to, prm, grid, stream);
 }
 
 const char* attn_fwd_strerror(int status) {
