@@ -27,6 +27,7 @@ SIGNATURES = {
     "attn_probe": {
         "attn_probe_mma_ss": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _vp, _vp]),
         "attn_probe_mma_ts": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+        "attn_probe_wait_timeout": (_c_int, [ctypes.c_ulonglong, ctypes.c_ulonglong, _vp, _vp, _vp]),
     },
 }
 

@@ -170,6 +170,37 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// One warp waits on an mbarrier that nothing ever arrives on, with the same
+// bounded wait the attention kernel uses; it must give up after timeout_ns and
+// report it (status = 1) instead of hanging.  A second warp raises the abort
+// flag instead when abort_after_ns > 0, and the waiter must see it (status = 2).
+__global__ void __launch_bounds__(64, 1) probe_wait_timeout_kernel(uint64_t timeout_ns, uint64_t abort_after_ns,
+                                                                   int* status, unsigned long long* waited_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const uint64_t t0 = global_timer_ns();
+    const bool ok = mbar_wait_bounded(&bar, 0, &abort_flag, timeout_ns);
+    const uint64_t t1 = global_timer_ns();
+    if (threadIdx.x == 0) {
+      *status = ok ? 0 : (abort_flag ? 2 : 1);
+      *waited_ns = t1 - t0;
+    }
+  } else if (abort_after_ns > 0 && threadIdx.x == 32) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < abort_after_ns) {
+    }
+    *reinterpret_cast<volatile uint32_t*>(&abort_flag) = 1;
+  }
+  __syncthreads();
+}
+
 int launch_status(cudaError_t e) { return e == cudaSuccess ? 0 : 100 + static_cast<int>(e); }
 
 }  // namespace
@@ -202,6 +233,14 @@ int attn_probe_mma_ts(const void* p, const void* v, int D, int lbo, int sbo, flo
   if (e != cudaSuccess) return launch_status(e);
   probe_mma_ts_kernel<<<1, 128, smem, stream>>>(tv, static_cast<const uint32_t*>(p), D, static_cast<uint32_t>(lbo),
                                                 static_cast<uint32_t>(sbo), o_out, status);
+  return launch_status(cudaGetLastError());
+}
+
+int attn_probe_wait_timeout(unsigned long long timeout_ns, unsigned long long abort_after_ns, int* status,
+                            unsigned long long* waited_ns, cudaStream_t stream) {
+  if (!status || !waited_ns) return 2;
+  if (timeout_ns == 0 || timeout_ns > 2000000000ull || abort_after_ns > 2000000000ull) return 1;
+  probe_wait_timeout_kernel<<<1, 64, 0, stream>>>(timeout_ns, abort_after_ns, status, waited_ns);
   return launch_status(cudaGetLastError());
 }
 

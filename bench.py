@@ -143,6 +143,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ----------------------------------------------------------------------------- multi-rank
+def reduce_max(x: float, dist, device) -> float:
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flop_per_rank_step: float, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return world * flop_per_rank_step * steps / (max_ms * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- timing
 def time_kernel(fn, steps: int, warmup: int, flush: torch.Tensor, stream) -> list[float]:
     """Per-step kernel time (ms) with CUDA events on the launching stream; L2 flushed before each step."""
@@ -199,8 +214,8 @@ def cpu_baseline(w: Workload, budget_s: float = 12.0) -> dict:
         if dt < budget_s / 8:
             chunk = min(chunk * 2, w.Sq)
     return {"value": flops / elapsed / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{nrows} query rows drawn uniformly per (batch, head) of the {w.name} workload "
-                      f"({flops:.3g} FLOP, {elapsed:.1f} s, fp64)"}
+            "sample": f"{nrows} query rows in total, drawn uniformly per (batch, head) in rounds, of the {w.name} "
+                      f"workload ({flops:.3g} FLOP, {elapsed:.1f} s, fp64)"}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -268,14 +283,10 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     st, site = ops.debug_status(stream)
     if st != ops.ATTN_OK:
         raise RuntimeError(f"kernel wait ran out (site {site})")
-    total_ms = sum(times)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(sum(times), dist, dev)
     ms_per_step = total_ms / args.steps
     flops = alg_flops(w)
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(flops, world, args.steps, total_ms)
 
     # end to end through the public API: pinned host inputs -> HBM -> kernel -> host outputs
     def e2e_step():
@@ -298,12 +309,8 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = reduce_max(e0.elapsed_time(e1), dist, dev)
+    e2e_value = job_tflops(flops, world, e2e_steps, e2e_ms)
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
     d2h = oh.numel() * oh.element_size() + lseh.numel() * lseh.element_size()
 
@@ -319,7 +326,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         "config": {"workload": w.label(), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
                    "causal": w.causal, "flop_count": "algorithmic: 4*D per unmasked (row, key) pair",
                    "alg_flop_per_step": flops, "conv_flop_per_step": conv_flops(w),
-                   "tflops_conv": world * conv_flops(w) * args.steps / (total_ms * 1e-3) / 1e12,
+                   "tflops_conv": job_tflops(conv_flops(w), world, args.steps, total_ms),
                    "pct_of_peak": 100.0 * achieved / peak,
                    "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

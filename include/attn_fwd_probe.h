@@ -40,6 +40,17 @@ int attn_probe_mma_ss(const void* q, int q_rows, const void* k, int k_rows, int 
 int attn_probe_mma_ts(const void* p, const void* v, int D, int lbo, int sbo, float* o_out, int* status,
                       cudaStream_t stream);
 
+/*
+ * Failure handling of the bounded waits, without faulting or hanging the GPU:
+ * one warp waits on an mbarrier that nothing arrives on, using the wait the
+ * attention kernel uses.  It must give up after timeout_ns (1 ns .. 2 s) and
+ * write *status = 1, or, when abort_after_ns > 0, see the abort flag another
+ * warp raises after that time and write *status = 2.  *waited_ns receives how
+ * long the wait lasted (device %globaltimer).  status, waited_ns: device memory.
+ */
+int attn_probe_wait_timeout(unsigned long long timeout_ns, unsigned long long abort_after_ns, int* status,
+                            unsigned long long* waited_ns, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
