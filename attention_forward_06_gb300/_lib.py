@@ -23,6 +23,10 @@ SIGNATURES = {
         "attn_fwd_strerror": (ctypes.c_char_p, [_c_int]),
         "attn_fwd_version": (_c_int, []),
         "attn_fwd_debug_status": (_c_int, [_vp, ctypes.POINTER(_c_int)]),
+        "attn_fwd_splitkv": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _vp,
+                                                                                  ctypes.c_size_t, _vp]),
+        "attn_fwd_splitkv_workspace_size": (ctypes.c_size_t, [_c_int] * 5),
+        "attn_fwd_splitkv_suggest": (_c_int, [_c_int] * 6),
     },
     "attn_probe": {
         "attn_probe_mma_ss": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _vp, _vp]),

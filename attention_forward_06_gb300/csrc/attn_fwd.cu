@@ -101,22 +101,41 @@ struct Params {
   int diag;
   int n_qblocks;  // ceil(Sq / ROWS_PER_ITEM)
   int BH;         // B * Hq
-  int n_items;    // BH * n_qblocks
+  int n_items;    // BH * n_qblocks (* n_splits)
   float c;        // scale * log2(e)
+  // split-key mode: the key tiles of each (b, h, query block) are cut into n_splits
+  // contiguous ranges; each writes an fp32 partial O and LSE for the merge
+  int n_splits;
+  float* o_part;    // [n_splits][BH][Sq][D]
+  float* lse_part;  // [n_splits][BH][Sq]
 };
 
 struct Item {
   int bh;       // b * Hq + query head
   int kv_z;     // b * Hkv + kv head
   int q0;       // first query row
+  int j0;       // first key tile
   int n_tiles;  // key tiles to visit
+  int split;    // key range index (split-key mode)
 };
 
-// Item x of the heaviest-first list: query block from the last, heads fastest.
+// Item x of the heaviest-first list: query block from the last, then (split-key
+// mode) the key range, heads fastest.
+template <bool SPLIT>
 __device__ __forceinline__ Item item_at(const Params& p, int x) {
   Item it;
-  const int qb = p.n_qblocks - 1 - x / p.BH;
-  it.bh = x % p.BH;
+  int qb, r;
+  if (SPLIT) {
+    const int per = p.BH * p.n_splits;
+    qb = p.n_qblocks - 1 - x / per;
+    r = x % per;
+    it.split = r / p.BH;
+    it.bh = r % p.BH;
+  } else {
+    qb = p.n_qblocks - 1 - x / p.BH;
+    it.bh = x % p.BH;
+    it.split = 0;
+  }
   const int b = it.bh / p.Hq;
   const int hq = it.bh % p.Hq;
   it.kv_z = b * p.Hkv + hq / p.G;
@@ -126,7 +145,14 @@ __device__ __forceinline__ Item item_at(const Params& p, int x) {
     const int last_row = min(it.q0 + ROWS_PER_ITEM, p.Sq) - 1;
     kv_end = min(p.Sk, last_row + p.diag + 1);
   }
-  it.n_tiles = kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
+  const int n_full = kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
+  if (SPLIT) {
+    it.j0 = static_cast<int>(static_cast<int64_t>(it.split) * n_full / p.n_splits);
+    it.n_tiles = static_cast<int>(static_cast<int64_t>(it.split + 1) * n_full / p.n_splits) - it.j0;
+  } else {
+    it.j0 = 0;
+    it.n_tiles = n_full;
+  }
   return it;
 }
 
@@ -157,7 +183,7 @@ __device__ __forceinline__ void record_abort(volatile uint32_t* abort_flag, int 
   atomicCAS(&g_status, 0, site);
 }
 
-template <int D>
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -222,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; ok; ++k) {
       const int x = item_index(p, k);
       if (x < 0) break;
-      const Item it = item_at(p, x);
+      const Item it = item_at<SPLIT>(p, x);
       if (it.n_tiles == 0) continue;
       if (q_issued > 0) {  // the previous item's last S has finished reading Q
         ok = warp_wait(&q_empty, (q_issued - 1) & 1, abort_v, kTimeoutNs);
@@ -248,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < D / 64; ++cb)
           tma_load_3d_elect(kv_s + slot * C::kTileBytes + cb * C::kColBlockBytes, map, &kv_full[slot], cb * 64,
-                            (i >> 1) * BN, it.kv_z);
+                            (it.j0 + (i >> 1)) * BN, it.kv_z);
         ++kv_it;
       }
     }
@@ -295,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; ok; ++k) {
       const int x = item_index(p, k);
       if (x < 0) break;
-      const Item it = item_at(p, x);
+      const Item it = item_at<SPLIT>(p, x);
       const int n = it.n_tiles;
       if (n == 0) continue;
       ok = warp_wait(&q_full, n_done & 1, abort_v, kTimeoutNs);
@@ -369,17 +395,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; ok; ++k) {
       const int x = item_index(p, k);
       if (x < 0) break;
-      const Item it = item_at(p, x);
+      const Item it = item_at<SPLIT>(p, x);
       const int row = it.q0 + t * BM + quarter * 32 + lane;  // global query row
       const bool live = row < p.Sq;
       __nv_bfloat16* orow = p.o + (static_cast<int64_t>(it.bh) * p.Sq + row) * D;
       float* lrow = p.lse + static_cast<int64_t>(it.bh) * p.Sq + row;
-      if (it.n_tiles == 0) {  // no key is visible to any row of this item
+      // split-key mode: this item's partial result rows
+      const int64_t prow = (static_cast<int64_t>(it.split) * p.BH + it.bh) * p.Sq + row;
+      if (it.n_tiles == 0) {  // no key is visible to any row of this item (or its key range is empty)
         if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(orow);
+          if (SPLIT) {
+            float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
 #pragma unroll
-          for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0u, 0u, 0u, 0u);
-          *lrow = -INFINITY;
+            for (int v4 = 0; v4 < D / 4; ++v4) dst[v4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            p.lse_part[prow] = -INFINITY;
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+            for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0u, 0u, 0u, 0u);
+            *lrow = -INFINITY;
+          }
         }
         continue;
       }
@@ -400,8 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint32_t r[128];
         tmem_ld128_wait(s_tmem, r);
-        if (j * BN + BN - 1 > lim_tile) {  // tile straddles the diagonal or the end of K
-          const int kmax = lim - j * BN;
+        const int jg = it.j0 + j;            // key tile index within the head
+        if (jg * BN + BN - 1 > lim_tile) {  // tile straddles the diagonal or the end of K
+          const int kmax = lim - jg * BN;
 #pragma unroll
           for (int i = 0; i < 128; ++i) r[i] = (i > kmax) ? __float_as_uint(-INFINITY) : r[i];
         }
@@ -510,6 +546,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&o_empty[t]);  // O_t may now be overwritten by the next item's first P.V
       const bool any_key = l > 0.0f;
       const float inv_l = any_key ? 1.0f / l : 0.0f;
+      if (SPLIT) {  // fp32 partial O (normalised by this range's l) and partial LSE, for the merge
+        if (live) {
+          const uint64_t s2 = f2_pack(inv_l, inv_l);
+          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll
+          for (int v4 = 0; v4 < D / 4; ++v4) {
+            float x0, x1, x2, x3;
+            f2_unpack(fmul2(f2_pack(__uint_as_float(o[4 * v4]), __uint_as_float(o[4 * v4 + 1])), s2), x0, x1);
+            f2_unpack(fmul2(f2_pack(__uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3])), s2), x2, x3);
+            dst[v4] = make_float4(x0, x1, x2, x3);
+          }
+          p.lse_part[prow] = any_key ? (m + lg2_approx(l_exact)) * 0.69314718055994531f : -INFINITY;
+        }
+        continue;
+      }
       // the staging buffer: with one buffer the Q tiles take turns (tile 0, then tile 1, per item)
       const int sb = (C::kStageBufs == 1) ? 0 : t;
       uint8_t* stage = st_s + sb * C::kStageBytes;
@@ -601,10 +652,16 @@ int prepare_device(int dev) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e);
   g_dev_sms[dev] = sms;
-  e = cudaFuncSetAttribute(attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(attn_fwd_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<128>::kSmemBytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<128>::kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_fwd_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<64>::kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_fwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<64>::kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e);
   if (!attn_host::encode_tiled_fn()) return ATTN_ERR_TENSOR_MAP;
@@ -618,38 +675,86 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
+bool misaligned(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; }
+
+constexpr int kMaxSplits = 256;
+
+// Merge of split-key partials (split-key mode): one warp per query row.
+//   LSE = ln sum_r exp(LSE_r);  O = sum_r exp(LSE_r - LSE) O_r   (rows whose every LSE_r is -inf: O = 0)
+// The weights are the exact probability mass of each key range; each O_r is
+// already normalised within its range.
 template <int D>
-int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-           const Params& prm, int grid, cudaStream_t stream) {
-  attn_fwd_kernel<D><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
-  const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+__global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict__ o_part,
+                                                         const float* __restrict__ lse_part,
+                                                         __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                                         int64_t rows, int n_splits) {
+  constexpr int kPerLane = D / 32;  // 4 (D = 128) or 2 (D = 64) consecutive columns per lane
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= rows) return;
+  float mx = -INFINITY;
+  for (int r = 0; r < n_splits; ++r) mx = fmaxf(mx, lse_part[r * rows + row]);
+  float acc[kPerLane];
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) acc[i] = 0.0f;
+  float total = 0.0f;
+  if (mx != -INFINITY) {
+    for (int r = 0; r < n_splits; ++r) {
+      const float w = expf(lse_part[r * rows + row] - mx);
+      total += w;
+      const float* src = o_part + (r * rows + row) * D + lane * kPerLane;
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) acc[i] += w * src[i];
+    }
+  }
+  const float inv = total > 0.0f ? 1.0f / total : 0.0f;
+  __nv_bfloat16* dst = o + row * D + lane * kPerLane;
+#pragma unroll
+  for (int i = 0; i < kPerLane; i += 2) {
+    const uint32_t w2 = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
+    *reinterpret_cast<uint32_t*>(dst + i) = w2;
+  }
+  if (lane == 0) lse[row] = mx == -INFINITY ? -INFINITY : mx + logf(total);
 }
 
-}  // namespace
+// Bytes of the split-key workspace: fp32 partial O, then (256-byte aligned) fp32 partial LSE.
+size_t splitkv_bytes(int64_t rows, int D, int n_splits, size_t* lse_offset) {
+  const size_t o_bytes = static_cast<size_t>(n_splits) * rows * D * 4;
+  const size_t off = (o_bytes + 255) & ~static_cast<size_t>(255);
+  if (lse_offset) *lse_offset = off;
+  return off + static_cast<size_t>(n_splits) * rows * 4;
+}
 
-extern "C" {
+// Everything a launch needs, after the host-side checks.
+struct Launch {
+  CUtensorMap tq, tk, tv, to;
+  Params prm;
+  int grid = 0;
+  int dev = 0;
+  bool empty = false;  // B == 0 or Sq == 0: nothing to do
+};
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
-             int Sk, int D, int causal, float scale, cudaStream_t stream) {
+int prepare_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+                   int Sk, int D, int causal, float scale, int n_splits, Launch* L) {
   // ---- argument checks (host only, before any CUDA call)
   if (B < 0 || Sq < 0 || Sk < 0 || Hq < 1 || Hkv < 1) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (causal < 0 || causal > 2) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (n_splits < 1 || n_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
   const int64_t q_elems = static_cast<int64_t>(B) * Hq * Sq * D;
   const int64_t kv_elems = static_cast<int64_t>(B) * Hkv * Sk * D;
   const int64_t rows = static_cast<int64_t>(B) * Hq * Sq;
   if (static_cast<int64_t>(B) * Hq > INT32_MAX || static_cast<int64_t>(B) * Hkv > INT32_MAX)
     return ATTN_ERR_INVALID_ARG;
-  if (B == 0 || Sq == 0) return ATTN_OK;  // nothing to compute
+  L->empty = (B == 0 || Sq == 0);
+  if (L->empty) return ATTN_OK;  // nothing to compute
   const int64_t n_qblocks = (Sq + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM;
-  const int64_t grid64 = static_cast<int64_t>(B) * Hq * n_qblocks;
-  if (grid64 > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+  const int64_t items = static_cast<int64_t>(B) * Hq * n_qblocks * n_splits;
+  if (items > INT32_MAX) return ATTN_ERR_INVALID_ARG;
   if (!q || !o || !lse) return ATTN_ERR_NULL_PTR;
   if (Sk > 0 && (!k || !v)) return ATTN_ERR_NULL_PTR;
-  auto misaligned = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
   if (misaligned(q) || misaligned(o) || misaligned(lse)) return ATTN_ERR_MISALIGNED;
   if (Sk > 0 && (misaligned(k) || misaligned(v))) return ATTN_ERR_MISALIGNED;
   const size_t qb = static_cast<size_t>(q_elems) * 2, kvb = static_cast<size_t>(kv_elems) * 2;
@@ -659,25 +764,25 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
     return ATTN_ERR_INVALID_ARG;
 
   // ---- device
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&L->dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  int st = prepare_device(dev);
+  const int st = prepare_device(L->dev);
   if (st != ATTN_OK) return st;
 
-  // ---- TMA maps: Q [B*Hq][Sq][D], K/V [B*Hkv][Sk][D]; boxes of 64 columns x 128 rows
-  CUtensorMap tq, tk, tv, to;
-  if (!attn_host::encode_bf16_rows(&tq, q, D, Sq, static_cast<uint64_t>(B) * Hq, BM)) return ATTN_ERR_TENSOR_MAP;
-  if (!attn_host::encode_bf16_rows(&to, o, D, Sq, static_cast<uint64_t>(B) * Hq, BM)) return ATTN_ERR_TENSOR_MAP;
+  // ---- TMA maps: Q, O [B*Hq][Sq][D], K/V [B*Hkv][Sk][D]; boxes of 64 columns x 128 rows
+  if (!attn_host::encode_bf16_rows(&L->tq, q, D, Sq, static_cast<uint64_t>(B) * Hq, BM)) return ATTN_ERR_TENSOR_MAP;
+  if (!attn_host::encode_bf16_rows(&L->to, o, D, Sq, static_cast<uint64_t>(B) * Hq, BM)) return ATTN_ERR_TENSOR_MAP;
   if (Sk > 0) {
-    if (!attn_host::encode_bf16_rows(&tk, k, D, Sk, static_cast<uint64_t>(B) * Hkv, BN)) return ATTN_ERR_TENSOR_MAP;
-    if (!attn_host::encode_bf16_rows(&tv, v, D, Sk, static_cast<uint64_t>(B) * Hkv, BN)) return ATTN_ERR_TENSOR_MAP;
+    if (!attn_host::encode_bf16_rows(&L->tk, k, D, Sk, static_cast<uint64_t>(B) * Hkv, BN))
+      return ATTN_ERR_TENSOR_MAP;
+    if (!attn_host::encode_bf16_rows(&L->tv, v, D, Sk, static_cast<uint64_t>(B) * Hkv, BN))
+      return ATTN_ERR_TENSOR_MAP;
   } else {
-    tk = tq;  // never read: every row is fully masked and no key tile is loaded
-    tv = tq;
+    L->tk = L->tq;  // never read: every row is fully masked and no key tile is loaded
+    L->tv = L->tq;
   }
 
-  Params prm;
+  Params& prm = L->prm;
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
   prm.Hq = Hq;
@@ -689,11 +794,92 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   prm.diag = causal == 1 ? Sk - Sq : 0;
   prm.n_qblocks = static_cast<int>(n_qblocks);
   prm.BH = B * Hq;
-  prm.n_items = static_cast<int>(grid64);
+  prm.n_items = static_cast<int>(items);
   prm.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  prm.n_splits = n_splits;
+  prm.o_part = nullptr;
+  prm.lse_part = nullptr;
   // persistent: one CTA per SM (shared memory and TMEM allow no second), never more CTAs than items
-  const int grid = static_cast<int>(grid64 < g_dev_sms[dev] ? grid64 : g_dev_sms[dev]);
-  return D == 128 ? launch<128>(tq, tk, tv, to, prm, grid, stream) : launch<64>(tq, tk, tv, to, prm, grid, stream);
+  L->grid = static_cast<int>(items < g_dev_sms[L->dev] ? items : g_dev_sms[L->dev]);
+  return ATTN_OK;
+}
+
+template <int D, bool SPLIT>
+int launch(const Launch& L, cudaStream_t stream) {
+  attn_fwd_kernel<D, SPLIT><<<L.grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(L.tq, L.tk, L.tv, L.to, L.prm);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+template <int D>
+int launch_merge(const Launch& L, int64_t rows, cudaStream_t stream) {
+  const int64_t blocks = (rows + 7) / 8;
+  attn_merge_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(L.prm.o_part, L.prm.lse_part, L.prm.o,
+                                                                           L.prm.lse, rows, L.prm.n_splits);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+// Split-key forward with the partials in `ws` (device memory, at least splitkv_bytes).
+int run_splitkv(const Launch& L0, void* ws, int64_t rows, int D, cudaStream_t stream) {
+  Launch L = L0;
+  size_t lse_off = 0;
+  splitkv_bytes(rows, D, L.prm.n_splits, &lse_off);
+  L.prm.o_part = static_cast<float*>(ws);
+  L.prm.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + lse_off);
+  int st = D == 128 ? launch<128, true>(L, stream) : launch<64, true>(L, stream);
+  if (st != ATTN_OK) return st;
+  return D == 128 ? launch_merge<128>(L, rows, stream) : launch_merge<64>(L, rows, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+             int Sk, int D, int causal, float scale, cudaStream_t stream) {
+  Launch L;
+  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, 1, &L);
+  if (st != ATTN_OK || L.empty) return st;
+  return D == 128 ? launch<128, false>(L, stream) : launch<64, false>(L, stream);
+}
+
+size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Sq, int D, int n_splits) {
+  if (B < 0 || Hq < 0 || Sq < 0 || (D != 64 && D != 128) || n_splits < 1 || n_splits > kMaxSplits) return 0;
+  return splitkv_bytes(static_cast<int64_t>(B) * Hq * Sq, D, n_splits, nullptr);
+}
+
+int attn_fwd_splitkv_suggest(int B, int Hq, int Sq, int Sk, int D, int causal) {
+  if (B < 1 || Hq < 1 || Sq < 1 || Sk < 1 || (D != 64 && D != 128) || causal < 0 || causal > 2) return 1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || prepare_device(dev) != ATTN_OK) return 1;
+  const int64_t items = static_cast<int64_t>(B) * Hq * ((Sq + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM);
+  const int64_t sms = g_dev_sms[dev];
+  if (items >= sms) return 1;
+  const int64_t tiles = (Sk + BN - 1) / BN;
+  int64_t splits = (2 * sms + items - 1) / items;     // about two items per SM
+  splits = splits < tiles / 4 ? splits : tiles / 4;   // at least four key tiles per range
+  splits = splits > kMaxSplits ? kMaxSplits : splits;
+  return static_cast<int>(splits < 1 ? 1 : splits);
+}
+
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Sq, int Sk, int D, int causal, float scale, int n_splits, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
+  Launch L;
+  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, n_splits, &L);
+  if (st != ATTN_OK || L.empty) return st;
+  const int64_t rows = static_cast<int64_t>(B) * Hq * Sq;
+  if (!workspace) return ATTN_ERR_NULL_PTR;
+  if (misaligned(workspace)) return ATTN_ERR_MISALIGNED;
+  const size_t need = splitkv_bytes(rows, D, n_splits, nullptr);
+  if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  const size_t qb = static_cast<size_t>(rows) * D * 2;
+  const size_t kvb = static_cast<size_t>(B) * Hkv * Sk * D * 2;
+  if (overlaps(workspace, need, q, qb) || overlaps(workspace, need, k, kvb) || overlaps(workspace, need, v, kvb) ||
+      overlaps(workspace, need, o, qb) || overlaps(workspace, need, lse, static_cast<size_t>(rows) * 4))
+    return ATTN_ERR_INVALID_ARG;
+  return run_splitkv(L, workspace, rows, D, stream);
 }
 
 const char* attn_fwd_strerror(int status) {

@@ -78,6 +78,47 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: int = 1,
     return o, lse
 
 
+def splitkv_workspace_size(B: int, Hq: int, Sq: int, D: int, n_splits: int) -> int:
+    return int(load().attn_fwd_splitkv_workspace_size(B, Hq, Sq, D, n_splits))
+
+
+def splitkv_suggest(B: int, Hq: int, Sq: int, Sk: int, D: int, causal: int) -> int:
+    return int(load().attn_fwd_splitkv_suggest(B, Hq, Sq, Sk, D, causal))
+
+
+def attn_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: int = 1, scale: float | None = None,
+                     n_splits: int | None = None, workspace: torch.Tensor | None = None,
+                     o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """Split-key forward (same result as ``attn_fwd``): ``(o, lse)``.
+
+    ``n_splits`` defaults to ``splitkv_suggest``; ``workspace`` (a CUDA tensor of at
+    least ``splitkv_workspace_size`` bytes) is allocated here when not given.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-d bf16 CUDA tensor")
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if n_splits is None:
+        n_splits = splitkv_suggest(B, Hq, Sq, Sk, D, int(causal))
+    need = splitkv_workspace_size(B, Hq, Sq, D, n_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                   B, Hq, Hkv, Sq, Sk, D, int(causal), ctypes.c_float(scale), int(n_splits),
+                                   workspace.data_ptr(), ws_bytes, _stream_handle(stream)))
+    return o, lse
+
+
 def debug_status(stream=None) -> tuple[int, int]:
     """Synchronise ``stream`` and read/clear the kernel's timeout word: ``(status, site)``."""
     site = ctypes.c_int(0)

@@ -45,6 +45,7 @@
 #define ATTN_FWD_H
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -70,6 +71,38 @@ extern "C" {
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
              int Sk, int D, int causal, float scale, cudaStream_t stream);
+
+/*
+ * Split-key forward: the same operation and result as attn_fwd, for shapes
+ * with too few (batch, head, 256-row query block) work items to fill the GPU
+ * (a short query chunk against a long key/value cache).  The visible key tiles
+ * of every work item are cut into n_splits contiguous ranges processed as
+ * separate items; each range writes its partial O (fp32, normalised within the
+ * range) and partial LSE into `workspace`, and a second kernel merges them:
+ *     LSE = ln sum_r exp(LSE_r),   O = sum_r exp(LSE_r - LSE) O_r.
+ * This is the log-sum-exp identity of the closed-form softmax normaliser (page
+ * "AdaSplash-2: Faster Differentiable Sparse Attention", technical summary
+ * section 1) applied to a partition of the keys.
+ *
+ * workspace: caller-owned device memory, 16-byte aligned, at least
+ * attn_fwd_splitkv_workspace_size(B, Hq, Sq, D, n_splits) bytes, not overlapping
+ * any input or output; its contents are overwritten.  1 <= n_splits <= 256.
+ * Two kernels are enqueued on `stream`; nothing is allocated.  Other arguments,
+ * layouts and status codes as attn_fwd (ATTN_ERR_INVALID_ARG also for a
+ * too-small workspace).
+ */
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Sq, int Sk, int D, int causal, float scale, int n_splits, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes attn_fwd_splitkv needs: n_splits * B*Hq*Sq * (D + 1) * 4 plus
+   alignment; 0 for invalid sizes.  Host only, no CUDA call. */
+size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Sq, int D, int n_splits);
+
+/* A split count for the current device: 1 when B*Hq*ceil(Sq/256) work items
+   already fill its SMs, else enough ranges for about two items per SM, with at
+   least four 128-key tiles per range. */
+int attn_fwd_splitkv_suggest(int B, int Hq, int Sq, int Sk, int D, int causal);
 
 /* Text for a status code.  For ATTN_ERR_CUDA it names the CUDA error of the
    calling thread's most recent failing call. */

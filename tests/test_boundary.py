@@ -121,3 +121,26 @@ def test_nm_lists_c_symbols_unmangled(built):
     out = subprocess.run(["nm", "-D", "--defined-only", built["attn_fwd"]], capture_output=True, text=True).stdout
     for f in declared_functions(HEADERS["attn_fwd"]):
         assert re.search(rf"\bT {f}$", out, flags=re.M), f
+
+
+def test_splitkv_workspace_size_formula():
+    for B, Hq, Sq, D, s in ((1, 2, 128, 64, 4), (2, 32, 513, 128, 7), (1, 1, 1, 128, 1)):
+        rows = B * Hq * Sq
+        o_bytes = s * rows * D * 4
+        expect = ((o_bytes + 255) // 256) * 256 + s * rows * 4
+        assert ops.splitkv_workspace_size(B, Hq, Sq, D, s) == expect
+    assert ops.splitkv_workspace_size(1, 1, 1, 96, 1) == 0
+    assert ops.splitkv_workspace_size(1, 1, 1, 128, 0) == 0
+    assert ops.splitkv_workspace_size(1, 1, 1, 128, 257) == 0
+
+
+def test_splitkv_invalid_arguments_before_any_device_work():
+    lib = _lib.load()
+    W = 0x600000
+    for n_splits in (0, 257, -1):
+        assert lib.attn_fwd_splitkv(Q, K, V, O, L, 1, 4, 2, 64, 64, 128, 1, 0.1, n_splits, W, 1 << 30, None) == \
+            ops.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_splitkv(Q, K, V, O, L, 1, 4, 2, 64, 64, 96, 1, 0.1, 2, W, 1 << 30, None) == \
+        ops.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_splitkv(0, K, V, O, L, 1, 4, 2, 64, 64, 128, 1, 0.1, 2, W, 1 << 30, None) == \
+        ops.ATTN_ERR_NULL_PTR
