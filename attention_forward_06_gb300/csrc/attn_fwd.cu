@@ -834,6 +834,34 @@ int run_splitkv(const Launch& L0, void* ws, int64_t rows, int D, cudaStream_t st
 
 }  // namespace
 
+// Fixed scratch for attn_fwd_splitkv_noalloc: the split-key partials of callers
+// that cannot allocate device memory.  Every device that loads this library
+// holds these 32 MiB until the process exits.  Host code only uses the name to
+// look up the device address (cudaGetSymbolAddress), once per device.
+constexpr size_t kNoAllocScratchBytes = size_t{32} << 20;
+static __device__ __align__(256) unsigned char g_splitkv_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices];  // device address of g_splitkv_scratch, per device
+
+// Device address of the fixed scratch on `dev` (the current device); looked up on first use.
+int noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_splitkv_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return ATTN_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
@@ -880,6 +908,22 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
       overlaps(workspace, need, o, qb) || overlaps(workspace, need, lse, static_cast<size_t>(rows) * 4))
     return ATTN_ERR_INVALID_ARG;
   return run_splitkv(L, workspace, rows, D, stream);
+}
+
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                             int Hkv, int Sq, int Sk, int D, int causal, float scale, int n_splits,
+                             cudaStream_t stream) {
+  Launch L;
+  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, n_splits, &L);
+  if (st != ATTN_OK || L.empty) return st;
+  const int64_t rows = static_cast<int64_t>(B) * Hq * Sq;
+  if (splitkv_bytes(rows, D, n_splits, nullptr) > kNoAllocScratchBytes) return ATTN_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  const int sst = noalloc_scratch(L.dev, &scratch);
+  if (sst != ATTN_OK) return sst;
+  // Every partial row is written by the first kernel before the merge reads it,
+  // so what an earlier call left in the scratch is never read: nothing to clear.
+  return run_splitkv(L, scratch, rows, D, stream);
 }
 
 const char* attn_fwd_strerror(int status) {

@@ -119,6 +119,29 @@ def attn_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: 
     return o, lse
 
 
+def attn_fwd_splitkv_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: int = 1,
+                             scale: float | None = None, n_splits: int = 1, o: torch.Tensor | None = None,
+                             lse: torch.Tensor | None = None, stream=None):
+    """Split-key forward with the library's fixed scratch instead of a workspace: ``(o, lse)``.
+
+    For callers that get only their input and output buffers and may not allocate
+    device memory; ``o``/``lse`` should then be given.  Work beyond the fixed
+    scratch (32 MiB of partials) is rejected; overlapping calls on the GPU race.
+    """
+    B, Hq, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check(load().attn_fwd_splitkv_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                           B, Hq, Hkv, Sq, Sk, D, int(causal), ctypes.c_float(scale), int(n_splits),
+                                           _stream_handle(stream)))
+    return o, lse
+
+
 def debug_status(stream=None) -> tuple[int, int]:
     """Synchronise ``stream`` and read/clear the kernel's timeout word: ``(status, site)``."""
     site = ctypes.c_int(0)

@@ -104,6 +104,30 @@ size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Sq, int D, int n_split
    least four 128-key tiles per range. */
 int attn_fwd_splitkv_suggest(int B, int Hq, int Sq, int Sk, int D, int causal);
 
+/*
+ * attn_fwd_splitkv without a workspace argument, for callers that cannot
+ * allocate device memory: code that is handed only its input and output
+ * buffers (an operator or plugin interface with no workspace) and must not
+ * call cudaMalloc itself, because a raw cudaMalloc can synchronise the device
+ * and goes around the memory manager that owns the GPU's memory.  (There is no
+ * counterpart on the pages; this is a calling convention of this library.)
+ *
+ * Same operation, arguments, result and status codes as attn_fwd_splitkv.  The
+ * partials live in a fixed 32 MiB device array inside the library instead of a
+ * workspace: calls whose n_splits * B*Hq*Sq * (D + 1) * 4 bytes (plus up to 255
+ * bytes of alignment) exceed 32 MiB are rejected with ATTN_ERR_INVALID_ARG
+ * before any device work.  Nothing is allocated: every GPU that loads the
+ * library holds the 32 MiB until the process exits.  The first call on a device
+ * looks up the array's device address there (once; a host-side query), so make
+ * that first call before any stream capture.  All calls share the one array and
+ * each call overwrites what it needs (nothing has to start at zero), so calls
+ * that overlap on the GPU -- on different streams, or on the same device from
+ * different threads without ordering -- race and must be serialised by the caller.
+ */
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                             int Hkv, int Sq, int Sk, int D, int causal, float scale, int n_splits,
+                             cudaStream_t stream);
+
 /* Text for a status code.  For ATTN_ERR_CUDA it names the CUDA error of the
    calling thread's most recent failing call. */
 const char* attn_fwd_strerror(int status);
