@@ -73,6 +73,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s per wait
 constexpr uint64_t kDrainTimeoutNs = 500000000ull;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
+constexpr float kLazyMassLimit = 4294967296.0f; // largest tile P mass accepted without a row max (2^32)
 
 // Sites recorded in the device status word when a wait runs out.
 constexpr int kSiteProducer = 1;
@@ -441,75 +442,95 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 128; ++i) r[i] = (i > kmax) ? __float_as_uint(-INFINITY) : r[i];
         }
-        // row max: four independent chains of 3-input max
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+        // Lazy row max.  The exponentials are taken against the running max m
+        // first; the row max of the tile is only computed (and m raised) when that
+        // pass shows the tile's P mass above kLazyMassLimit, on the first tile of
+        // a row, or while a row has seen no key.  Any m is exact here: O and both
+        // normalisers share it, and P, l and O keep full relative precision at any
+        // magnitude, so a stale m only costs headroom (P stays below 2^32).
+        bool need_max = __any_sync(0xffffffffu, j == 0 || m == -INFINITY);
+        float tile_l = 0.0f, tile_le = 0.0f;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+          if (need_max) {
+            // row max: four independent chains of 3-input max
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 128; i += 8) {
-          mx0 = max3f(mx0, __uint_as_float(r[i + 0]), __uint_as_float(r[i + 1]));
-          mx1 = max3f(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-          mx2 = max3f(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
-          mx3 = max3f(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
-        }
-        const float m_tile = fmaxf(max3f(mx0, mx1, mx2), mx3) * c;
-        const bool raise = m_tile > m + kRescaleThreshold;
-        float alpha = 1.0f;
-        if (raise) {
-          alpha = ex2_approx(m - m_tile);
-          m = m_tile;
-          l *= alpha;
-          l_exact *= alpha;
-        }
-        if (j > 0 && __any_sync(0xffffffffu, raise)) {
-          // rescale this warp's 32 rows of O_t (PV_t(j-1) has completed: its commit preceded S_t(j)'s)
-          const uint64_t a2 = f2_pack(alpha, alpha);
+            for (int i = 0; i < 128; i += 8) {
+              mx0 = max3f(mx0, __uint_as_float(r[i + 0]), __uint_as_float(r[i + 1]));
+              mx1 = max3f(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+              mx2 = max3f(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+              mx3 = max3f(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+            }
+            const float m_tile = fmaxf(max3f(mx0, mx1, mx2), mx3) * c;
+            const bool raise = m_tile > m + kRescaleThreshold;
+            float alpha = 1.0f;
+            if (raise) {
+              alpha = ex2_approx(m - m_tile);
+              m = m_tile;
+              l *= alpha;
+              l_exact *= alpha;
+            }
+            if (j > 0 && __any_sync(0xffffffffu, raise)) {
+              // rescale this warp's 32 rows of O_t (PV_t(j-1) has completed: its commit preceded S_t(j)'s)
+              const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-          for (int cb = 0; cb < D / 32; ++cb) {
-            uint32_t o[32];
-            tmem_ld32_wait(o_tmem + cb * 32, o);
+              for (int cb = 0; cb < D / 32; ++cb) {
+                uint32_t o[32];
+                tmem_ld32_wait(o_tmem + cb * 32, o);
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
+                for (int i = 0; i < 32; i += 2) {
+                  float x0, x1;
+                  f2_unpack(fmul2(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), x0, x1);
+                  o[i] = __float_as_uint(x0);
+                  o[i + 1] = __float_as_uint(x1);
+                }
+                tmem_st32(o_tmem + cb * 32, o);
+              }
+            }
+          }
+          // P = exp2(s * c - m): packed FMA, one ex2 per element, bf16 pairs; two sums.
+          // A second pass overwrites the P of the first in TMEM (the MMA has not read it).
+          const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+          const uint64_t c2 = f2_pack(c, c);
+          const uint64_t nm2 = f2_pack(neg_m, neg_m);
+          uint64_t le0 = f2_pack(0.0f, 0.0f), le1 = le0;
+          float lr0 = 0.0f, lr1 = 0.0f, lr2 = 0.0f, lr3 = 0.0f;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int e = half * 64 + 2 * i;
               float x0, x1;
-              f2_unpack(fmul2(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), x0, x1);
-              o[i] = __float_as_uint(x0);
-              o[i + 1] = __float_as_uint(x1);
+              f2_unpack(ffma2(f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2), x0, x1);
+              const float p0 = ex2_approx(x0);
+              const float p1 = ex2_approx(x1);
+              pk[i] = pack_bf16x2(p0, p1);
+              if (i & 1) {
+                le1 = fadd2(le1, f2_pack(p0, p1));
+                add_bf16x2_to_f32(lr2, lr3, pk[i]);
+              } else {
+                le0 = fadd2(le0, f2_pack(p0, p1));
+                add_bf16x2_to_f32(lr0, lr1, pk[i]);
+              }
             }
-            tmem_st32(o_tmem + cb * 32, o);
+            tmem_st32(s_tmem + half * 32, pk);
           }
-        }
-        // P = exp2(s * c - m): packed FMA, one ex2 per element, bf16 pairs; two sums
-        const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-        const uint64_t c2 = f2_pack(c, c);
-        const uint64_t nm2 = f2_pack(neg_m, neg_m);
-        uint64_t le0 = f2_pack(0.0f, 0.0f), le1 = le0;
-        float lr0 = 0.0f, lr1 = 0.0f, lr2 = 0.0f, lr3 = 0.0f;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int e = half * 64 + 2 * i;
-            float x0, x1;
-            f2_unpack(ffma2(f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2), x0, x1);
-            const float p0 = ex2_approx(x0);
-            const float p1 = ex2_approx(x1);
-            pk[i] = pack_bf16x2(p0, p1);
-            if (i & 1) {
-              le1 = fadd2(le1, f2_pack(p0, p1));
-              add_bf16x2_to_f32(lr2, lr3, pk[i]);
-            } else {
-              le0 = fadd2(le0, f2_pack(p0, p1));
-              add_bf16x2_to_f32(lr0, lr1, pk[i]);
-            }
+          {
+            float a0, a1, b0, b1;
+            f2_unpack(le0, a0, a1);
+            f2_unpack(le1, b0, b1);
+            tile_le = (a0 + a1) + (b0 + b1);
+            tile_l = (lr0 + lr1) + (lr2 + lr3);
           }
-          tmem_st32(s_tmem + half * 32, pk);
+          if (need_max) break;
+          // NaN or overflow fails the comparison too
+          need_max = __any_sync(0xffffffffu, !(tile_le <= kLazyMassLimit));
+          if (!need_max) break;
         }
-        {
-          float a0, a1, b0, b1;
-          f2_unpack(le0, a0, a1);
-          f2_unpack(le1, b0, b1);
-          l_exact += (a0 + a1) + (b0 + b1);
-          l += (lr0 + lr1) + (lr2 + lr3);
-        }
+        l_exact += tile_le;
+        l += tile_l;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
