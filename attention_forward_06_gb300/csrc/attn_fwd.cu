@@ -27,16 +27,19 @@
 // have read O out of TMEM (o_empty), and the next item's Q only waits for the
 // last S of this one (q_empty).
 // TMEM columns: S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [384,384+D); P_t
-// (bf16 pairs) overwrites the first 64 columns of S_t once S_t is in registers.
+// (bf16 pairs) overwrites the last 64 columns of S_t once S_t is in registers,
+// so the S of the first 64 keys stays readable until the next S_t.
 //
-// Online softmax per row, in log2 units (c = scale * log2 e): the running max
-// m is only raised when a tile's max exceeds it by more than 8 (a factor 256);
-// otherwise the stale m stays, which is exact because O and the normalisers
-// share it.  l sums the bf16-rounded P values the tensor cores multiply, so the
-// final O / l is a convex combination of V rows; a second, fp32 sum of the
-// unrounded P gives the LSE.  Causal masking touches only the tiles that
-// straddle the diagonal (or the ragged end of K); tiles wholly above the
-// diagonal are never loaded.
+// Online softmax per row, in log2 units (c = scale * log2 e), with a lazy
+// running max m: a tile's exponentials are taken against the current m, and
+// the tile's row max is only computed (and m raised, when it exceeds m by more
+// than 8) on a row's first tile or when the tile's P mass under the stale m
+// exceeds 2^32.  Any m is exact because O and the normalisers share it.  l sums
+// the bf16-rounded P values the tensor cores multiply (taken after P has been
+// handed to the MMA), so the final O / l is a convex combination of V rows; a
+// second, fp32 sum of the unrounded P gives the LSE.  Causal masking touches
+// only the tiles that straddle the diagonal (or the ragged end of K); tiles
+// wholly above the diagonal are never loaded.
 //
 // Every mbarrier wait is bounded: a wait that runs out sets a shared abort
 // flag and a device status word, and all roles unwind to the final barrier,
@@ -49,6 +52,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "attn_fwd.h"
 #include "host_util.h"
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t vd = sdesc_sw128(opaque(kv_addr) + slot * C::kTileBytes, C::kColBlockBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk)
-        mma_bf16_ts_elect(tmem + 2 * BN + t * 128, tmem + t * BN + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
+        mma_bf16_ts_elect(tmem + 2 * BN + t * 128, tmem + t * BN + 64 + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
                           (accumulate || kk > 0) ? 1u : 0u);
     };
     // wait for load number `n` of the K/V stream
@@ -437,103 +441,131 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r[128];
         tmem_ld128_wait(s_tmem, r);
         const int jg = it.j0 + j;            // key tile index within the head
-        if (jg * BN + BN - 1 > lim_tile) {  // tile straddles the diagonal or the end of K
-          const int kmax = lim - jg * BN;
+        const bool masked = jg * BN + BN - 1 > lim_tile;  // tile straddles the diagonal or the end of K
+        const int kmax = lim - jg * BN;
+        if (masked) {
 #pragma unroll
           for (int i = 0; i < 128; ++i) r[i] = (i > kmax) ? __float_as_uint(-INFINITY) : r[i];
         }
-        // Lazy row max.  The exponentials are taken against the running max m
-        // first; the row max of the tile is only computed (and m raised) when that
-        // pass shows the tile's P mass above kLazyMassLimit, on the first tile of
-        // a row, or while a row has seen no key.  Any m is exact here: O and both
-        // normalisers share it, and P, l and O keep full relative precision at any
-        // magnitude, so a stale m only costs headroom (P stays below 2^32).
-        bool need_max = __any_sync(0xffffffffu, j == 0 || m == -INFINITY);
-        float tile_l = 0.0f, tile_le = 0.0f;
-#pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
-          if (need_max) {
-            // row max: four independent chains of 3-input max
-            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+        // Row max of the tile; raises m (and rescales l, l_exact and O_t) when the
+        // tile's max exceeds it by more than kRescaleThreshold.
+        auto row_max = [&]() {
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 128; i += 8) {
-              mx0 = max3f(mx0, __uint_as_float(r[i + 0]), __uint_as_float(r[i + 1]));
-              mx1 = max3f(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-              mx2 = max3f(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
-              mx3 = max3f(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
-            }
-            const float m_tile = fmaxf(max3f(mx0, mx1, mx2), mx3) * c;
-            const bool raise = m_tile > m + kRescaleThreshold;
-            float alpha = 1.0f;
-            if (raise) {
-              alpha = ex2_approx(m - m_tile);
-              m = m_tile;
-              l *= alpha;
-              l_exact *= alpha;
-            }
-            if (j > 0 && __any_sync(0xffffffffu, raise)) {
-              // rescale this warp's 32 rows of O_t (PV_t(j-1) has completed: its commit preceded S_t(j)'s)
-              const uint64_t a2 = f2_pack(alpha, alpha);
+          for (int i = 0; i < 128; i += 8) {
+            mx0 = max3f(mx0, __uint_as_float(r[i + 0]), __uint_as_float(r[i + 1]));
+            mx1 = max3f(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+            mx2 = max3f(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+            mx3 = max3f(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+          }
+          const float m_tile = fmaxf(max3f(mx0, mx1, mx2), mx3) * c;
+          const bool raise = m_tile > m + kRescaleThreshold;
+          float alpha = 1.0f;
+          if (raise) {
+            alpha = ex2_approx(m - m_tile);
+            m = m_tile;
+            l *= alpha;
+            l_exact *= alpha;
+          }
+          if (j > 0 && __any_sync(0xffffffffu, raise)) {
+            // rescale this warp's 32 rows of O_t (PV_t(j-1) has completed: its commit preceded S_t(j)'s)
+            const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-              for (int cb = 0; cb < D / 32; ++cb) {
-                uint32_t o[32];
-                tmem_ld32_wait(o_tmem + cb * 32, o);
+            for (int cb = 0; cb < D / 32; ++cb) {
+              uint32_t o[32];
+              tmem_ld32_wait(o_tmem + cb * 32, o);
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                  float x0, x1;
-                  f2_unpack(fmul2(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), x0, x1);
-                  o[i] = __float_as_uint(x0);
-                  o[i + 1] = __float_as_uint(x1);
-                }
-                tmem_st32(o_tmem + cb * 32, o);
+              for (int i = 0; i < 32; i += 2) {
+                float x0, x1;
+                f2_unpack(fmul2(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), x0, x1);
+                o[i] = __float_as_uint(x0);
+                o[i + 1] = __float_as_uint(x1);
               }
+              tmem_st32(o_tmem + cb * 32, o);
             }
           }
-          // P = exp2(s * c - m): packed FMA, one ex2 per element, bf16 pairs; two sums.
-          // A second pass overwrites the P of the first in TMEM (the MMA has not read it).
+        };
+        // P = exp2(s * c - m) for one half of the keys: packed FMA, one ex2 per
+        // element, bf16 pairs into TMEM columns 64-127 of S_t (P over keys 0-63 then
+        // 64-127), and the fp32 sum of P.  The S values of keys 0-63 (TMEM columns
+        // 0-63) stay intact until the next S_t.
+        uint64_t le0, le1;
+        uint32_t pk0[32], pk1[32];
+        auto exp_half = [&](auto half_c, uint32_t(&pk)[32]) {
+          constexpr int half = decltype(half_c)::value;
           const float neg_m = (m == -INFINITY) ? 0.0f : -m;
           const uint64_t c2 = f2_pack(c, c);
           const uint64_t nm2 = f2_pack(neg_m, neg_m);
-          uint64_t le0 = f2_pack(0.0f, 0.0f), le1 = le0;
-          float lr0 = 0.0f, lr1 = 0.0f, lr2 = 0.0f, lr3 = 0.0f;
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t pk[32];
+          for (int i = 0; i < 32; ++i) {
+            const int e = half * 64 + 2 * i;
+            float x0, x1;
+            f2_unpack(ffma2(f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2), x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            pk[i] = pack_bf16x2(p0, p1);
+            if (i & 1)
+              le1 = fadd2(le1, f2_pack(p0, p1));
+            else
+              le0 = fadd2(le0, f2_pack(p0, p1));
+          }
+          tmem_st32(s_tmem + 64 + half * 32, pk);
+        };
+        auto tile_mass = [&]() {
+          float a0, a1, b0, b1;
+          f2_unpack(le0, a0, a1);
+          f2_unpack(le1, b0, b1);
+          return (a0 + a1) + (b0 + b1);
+        };
+        // Lazy row max.  The exponentials are taken against the running max m
+        // first; the row max of the tile is only computed (and m raised) on the
+        // first tile of a row, while a row has seen no key, or when that pass shows
+        // the tile's P mass above kLazyMassLimit.  Any m is exact here: O and both
+        // normalisers share it, and P, l and O keep full relative precision at any
+        // magnitude, so a stale m only costs headroom (P stays below 2^32).
+        const bool first = __any_sync(0xffffffffu, j == 0 || m == -INFINITY);
+        if (first) row_max();
+        le0 = f2_pack(0.0f, 0.0f);
+        le1 = le0;
+        exp_half(std::integral_constant<int, 0>{}, pk0);
+        exp_half(std::integral_constant<int, 1>{}, pk1);
+        float tile_le = tile_mass();
+        // NaN or overflow fails the comparison too
+        if (!first && __any_sync(0xffffffffu, !(tile_le <= kLazyMassLimit))) {
+          // rare: reload the S of keys 0-63 (P now sits over keys 64-127, whose S is
+          // still in registers), take the row max, and redo the exponentials
+          {
+            uint32_t s0[32], s1[32];
+            tmem_ld32_wait(s_tmem, s0);
+            tmem_ld32_wait(s_tmem + 32, s1);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const int e = half * 64 + 2 * i;
-              float x0, x1;
-              f2_unpack(ffma2(f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2), x0, x1);
-              const float p0 = ex2_approx(x0);
-              const float p1 = ex2_approx(x1);
-              pk[i] = pack_bf16x2(p0, p1);
-              if (i & 1) {
-                le1 = fadd2(le1, f2_pack(p0, p1));
-                add_bf16x2_to_f32(lr2, lr3, pk[i]);
-              } else {
-                le0 = fadd2(le0, f2_pack(p0, p1));
-                add_bf16x2_to_f32(lr0, lr1, pk[i]);
-              }
+              r[i] = (masked && i > kmax) ? __float_as_uint(-INFINITY) : s0[i];
+              r[32 + i] = (masked && 32 + i > kmax) ? __float_as_uint(-INFINITY) : s1[i];
             }
-            tmem_st32(s_tmem + half * 32, pk);
           }
-          {
-            float a0, a1, b0, b1;
-            f2_unpack(le0, a0, a1);
-            f2_unpack(le1, b0, b1);
-            tile_le = (a0 + a1) + (b0 + b1);
-            tile_l = (lr0 + lr1) + (lr2 + lr3);
-          }
-          if (need_max) break;
-          // NaN or overflow fails the comparison too
-          need_max = __any_sync(0xffffffffu, !(tile_le <= kLazyMassLimit));
-          if (!need_max) break;
+          row_max();
+          le0 = f2_pack(0.0f, 0.0f);
+          le1 = le0;
+          exp_half(std::integral_constant<int, 0>{}, pk0);
+          exp_half(std::integral_constant<int, 1>{}, pk1);
+          tile_le = tile_mass();
         }
         l_exact += tile_le;
-        l += tile_l;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
+        {  // the sum of the bf16-rounded P, after the hand-off (off the MMA's critical path)
+          float q0 = 0.0f, q1 = 0.0f, q2 = 0.0f, q3 = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            add_bf16x2_to_f32(q0, q1, pk0[i]);
+            add_bf16x2_to_f32(q2, q3, pk0[i + 1]);
+            add_bf16x2_to_f32(q0, q1, pk1[i]);
+            add_bf16x2_to_f32(q2, q3, pk1[i + 1]);
+          }
+          l += (q0 + q1) + (q2 + q3);
+        }
       }
       if (!ok) {
         if (lane == 0) record_abort(abort_v, kSiteSoftmax);

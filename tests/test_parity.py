@@ -68,6 +68,24 @@ def test_sharp_logits_online_rescale():
     full_check(1, 2, 2, 384, 384, 64, 0, seed=78, qk_std=3.0)
 
 
+@pytest.mark.parametrize("Sq,Sk,D,causal,boost", [
+    (256, 512, 128, 0, 20.0),    # a later key tile ~70 log2 units above the first: P mass far above 2^32
+    (384, 384, 64, 1, 100.0),    # first pass overflows to inf; the boosted tile is the diagonal (masked) one
+    (300, 700, 128, 1, 11.0),    # bottom-right, ragged; only part of the rows cross the limit, the rest keep P near 2^30
+])
+def test_lazy_max_second_pass(Sq, Sk, D, causal, boost):
+    # The kernel takes a tile's exponentials against the running max first and
+    # recomputes them with the tile's row max when the P mass exceeds 2^32; keys
+    # 256-383 (the third key tile) are scaled so that later tile dominates.
+    q, k, v = draw(1, 4, 2, Sq, Sk, D, seed=int(boost) + Sq)
+    k = k.clone()
+    k[:, :, 256:384] = (k[:, :, 256:384].float() * boost).to(torch.bfloat16)
+    scale = float(np.float32(D ** -0.5))
+    o, lse = run_gpu(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal, scale)
+    compare(o, lse, o_ref, lse_ref)
+
+
 def test_train_workload_full_oracle():
     w = WORKLOADS["train"]
     full_check(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.causal, w.seed, w.qk_std)
