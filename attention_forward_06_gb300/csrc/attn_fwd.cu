@@ -93,8 +93,14 @@ struct Cfg {
   static constexpr int kQBytes = QTILES * BM * D * 2;
   static constexpr int kStageBytes = BM * D * 2;           // one Q tile of O in bf16, 128-B swizzled
   static constexpr int kStageBufs = (D == 128) ? 1 : 2;    // O staging buffers (1: the two Q tiles take turns)
+  // D = 64: the P.V product is D + 16 columns wide, its last 16 columns multiplying
+  // P by a block of ones, so the tensor cores accumulate the rounded-P row sum l
+  // next to O (TMEM has room for it only at D = 64).
+  static constexpr bool kTensorRowSum = (D == 64);
+  static constexpr int kPvN = kTensorRowSum ? D + 16 : D;  // MMA N of the P.V product
+  static constexpr int kOnesBytes = kTensorRowSum ? BN * 128 : 0;  // 128 keys x 64 columns of bf16 1.0
   static constexpr int kSmemBytes =
-      kQBytes + kStages * kTileBytes + kStageBufs * kStageBytes + 1024;  // + alignment slack
+      kQBytes + kStages * kTileBytes + kStageBufs * kStageBytes + kOnesBytes + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -200,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* q_s = smem;               // Q tile t at q_s + t * kTileBytes
   uint8_t* kv_s = smem + C::kQBytes;  // slot s at kv_s + s * kTileBytes
   uint8_t* st_s = kv_s + S * C::kTileBytes;  // O staging buffer b at st_s + b * kStageBytes
+  uint8_t* ones_s = st_s + C::kStageBufs * C::kStageBytes;  // D = 64: the ones block of the row-sum columns
   __shared__ uint64_t kv_full[S], kv_empty[S];
   __shared__ uint64_t q_full, q_empty, s_full[QTILES], p_full[QTILES], o_final[QTILES], o_empty[QTILES];
   __shared__ uint64_t stage_rel[QTILES], mma_drain;
@@ -230,6 +237,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) {
     tmem_alloc(&tmem_base_slot, kTmemCols);
     tmem_relinquish();
+  }
+  if constexpr (C::kTensorRowSum) {
+    // bf16 1.0 everywhere (the swizzle does not matter for a constant block), made
+    // visible to the tensor cores' (async proxy) reads
+    for (int i = threadIdx.x; i < C::kOnesBytes / 16; i += kThreads)
+      reinterpret_cast<uint4*>(ones_s)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -293,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tcgen05 issuer
     const uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
-    const uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
+    const uint32_t idesc_pv = idesc_bf16_f32(BM, C::kPvN, true);
     const uint32_t q_addr = smem_u32(q_s);
     const uint32_t kv_addr = smem_u32(kv_s);
     // The whole warp runs the issue code (converged); one elected lane issues.
@@ -308,8 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_bf16_ss_elect(tmem + t * BN, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
     };
+    const uint32_t ones_addr = smem_u32(ones_s);
     auto issue_pv = [=](int t, uint32_t slot, bool accumulate) {
-      const uint64_t vd = sdesc_sw128(opaque(kv_addr) + slot * C::kTileBytes, C::kColBlockBytes, 1024);
+      // V is MN-major: the leading byte offset steps from one 64-column block of V to
+      // the next; at D = 64 the second block is the ones block (the row-sum columns)
+      const uint32_t v_addr = opaque(kv_addr) + slot * C::kTileBytes;
+      const uint64_t vd =
+          sdesc_sw128(v_addr, C::kTensorRowSum ? ones_addr - v_addr : C::kColBlockBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk)
         mma_bf16_ts_elect(tmem + 2 * BN + t * 128, tmem + t * BN + 64 + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
@@ -471,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // rescale this warp's 32 rows of O_t (PV_t(j-1) has completed: its commit preceded S_t(j)'s)
             const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-            for (int cb = 0; cb < D / 32; ++cb) {
+            for (int cb = 0; cb < (C::kPvN + 31) / 32; ++cb) {  // O and, at D = 64, the row-sum columns
               uint32_t o[32];
               tmem_ld32_wait(o_tmem + cb * 32, o);
 #pragma unroll
@@ -555,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
-        {  // the sum of the bf16-rounded P, after the hand-off (off the MMA's critical path)
+        if constexpr (!C::kTensorRowSum) {  // the sum of the bf16-rounded P, after the hand-off
           float q0 = 0.0f, q1 = 0.0f, q2 = 0.0f, q3 = 0.0f;
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
@@ -594,6 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           o[i] = lo[i];
           o[32 + i] = hi[i];
         }
+        l = __uint_as_float(tmem_ld1_wait(o_tmem + D));  // rounded-P row sum from the tensor cores
       }
       tc_fence_before();
       mbar_arrive(&o_empty[t]);  // O_t may now be overwritten by the next item's first P.V

@@ -380,6 +380,18 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
       : "memory");
 }
 
+// One column: this thread's lane of TMEM column `taddr`.
+__device__ __forceinline__ uint32_t tmem_ld1_wait(uint32_t taddr) {
+  uint32_t v;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v)
+      : "r"(taddr)
+      : "memory");
+  return v;
+}
+
 // 128 consecutive columns (four x32 loads issued back to back, one wait).
 __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, uint32_t (&r)[128]) {
   asm volatile(
