@@ -51,6 +51,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -119,6 +120,7 @@ struct Params {
   int n_splits;
   float* o_part;    // [n_splits][BH][Sq][D]
   float* lse_part;  // [n_splits][BH][Sq]
+  int sched_slot;   // counter pair of the dynamic schedule used by this launch
 };
 
 struct Item {
@@ -167,15 +169,18 @@ __device__ __forceinline__ Item item_at(const Params& p, int x) {
   return it;
 }
 
-// k-th item of this CTA (boustrophedon deal), or -1 past the end.
-__device__ __forceinline__ int item_index(const Params& p, int k) {
-  const int G = static_cast<int>(gridDim.x);
-  const int c = static_cast<int>(blockIdx.x);
-  const int x = k * G + ((k & 1) ? (G - 1 - c) : c);
-  return x < p.n_items ? x : -1;
-}
-
 __device__ int g_status;  // sticky: 0 = fine, else the site of the first wait that ran out
+
+// Dynamic schedule.  CTA c starts on item c; later items are claimed in list
+// order (heaviest first) from a counter, so a CTA that finishes early takes the
+// next item and the CTAs end within about one (small) item of each other.  Each
+// launch uses one of kSchedSlots counter pairs (claimed items, CTAs finished),
+// chosen by the host; the last CTA to finish returns its pair to zero.
+constexpr int kSchedSlots = 64;
+__device__ int g_sched_next[kSchedSlots];
+__device__ unsigned int g_sched_done[kSchedSlots];
+constexpr int kSeqSlots = 4;  // depth of the shared-memory ring through which the producer publishes items
+constexpr int kSeqConsumers = 9;  // warps reading the ring: eight softmax warps and the issuer
 
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -210,6 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t kv_full[S], kv_empty[S];
   __shared__ uint64_t q_full, q_empty, s_full[QTILES], p_full[QTILES], o_final[QTILES], o_empty[QTILES];
   __shared__ uint64_t stage_rel[QTILES], mma_drain;
+  __shared__ uint64_t seq_full[kSeqSlots], seq_empty[kSeqSlots];
+  __shared__ int item_seq[kSeqSlots];  // the CTA's k-th item at slot k % kSeqSlots (-1: no more)
   __shared__ uint32_t tmem_base_slot;
   __shared__ uint32_t abort_flag;
 
@@ -231,6 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&stage_rel[t], 1);
     }
     mbar_init(&mma_drain, 1);
+    for (int i = 0; i < kSeqSlots; ++i) {
+      mbar_init(&seq_full[i], 1);
+      mbar_init(&seq_empty[i], kSeqConsumers);
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -250,6 +261,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_slot;
   volatile uint32_t* abort_v = &abort_flag;
+  // k-th item of this CTA as published by the producer (-1: no more); false when a wait gave up
+  auto next_item = [&](int k, int& x) {
+    if (!warp_wait(&seq_full[k % kSeqSlots], (k / kSeqSlots) & 1, abort_v, kTimeoutNs)) return false;
+    x = *reinterpret_cast<volatile int*>(&item_seq[k % kSeqSlots]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&seq_empty[k % kSeqSlots]);
+    return true;
+  };
 
   if (warp >= 8) {
    // warpgroup 2: every warp shrinks its registers at the same instruction, then splits by role
@@ -264,11 +283,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t kv_it = 0;     // K/V loads issued so far (over all items)
     uint32_t q_issued = 0;  // Q loads issued so far (one per item with key tiles)
     bool ok = true;
+    int x = static_cast<int>(blockIdx.x);  // the first item is fixed; the rest are claimed
     for (int k = 0; ok; ++k) {
-      const int x = item_index(p, k);
-      if (x < 0) break;
+      const bool more = x < p.n_items;
+      // publish the item to the other roles
+      if (k >= kSeqSlots) {
+        ok = warp_wait(&seq_empty[k % kSeqSlots], (k / kSeqSlots - 1) & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        item_seq[k % kSeqSlots] = more ? x : -1;
+        mbar_arrive(&seq_full[k % kSeqSlots]);
+      }
+      __syncwarp();
+      if (!more) break;
       const Item it = item_at<SPLIT>(p, x);
-      if (it.n_tiles == 0) continue;
+      // The next item is claimed once this item's loads are all issued (about two
+      // key tiles before its end), so items are handed out in the order CTAs free up.
+      auto claim = [&]() {
+        int claimed = 0;
+        if (lane == 0) claimed = atomicAdd(&g_sched_next[p.sched_slot], 1);
+        return static_cast<int>(gridDim.x) + __shfl_sync(0xffffffffu, claimed, 0);
+      };
+      if (it.n_tiles == 0) {
+        x = claim();
+        continue;
+      }
       if (q_issued > 0) {  // the previous item's last S has finished reading Q
         ok = warp_wait(&q_empty, (q_issued - 1) & 1, abort_v, kTimeoutNs);
         if (!ok) break;
@@ -296,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (it.j0 + (i >> 1)) * BN, it.kv_z);
         ++kv_it;
       }
+      if (ok) x = claim();
     }
     if (!ok) {
       if (lane == 0) record_abort(abort_v, kSiteProducer);
@@ -343,8 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n_done = 0;  // items with key tiles processed
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int x = item_index(p, k);
-      if (x < 0) break;
+      int x;
+      ok = next_item(k, x);
+      if (!ok || x < 0) break;
       const Item it = item_at<SPLIT>(p, x);
       const int n = it.n_tiles;
       if (n == 0) continue;
@@ -417,7 +459,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
-      const int x = item_index(p, k);
+      int x;
+      ok = next_item(k, x);
+      if (!ok) {
+        if (lane == 0) record_abort(abort_v, kSiteSoftmax);
+        break;
+      }
       if (x < 0) break;
       const Item it = item_at<SPLIT>(p, x);
       const int row = it.q0 + t * BM + quarter * 32 + lane;  // global query row
@@ -690,6 +737,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (threadIdx.x == 0) {  // every claim of this CTA is done; the last CTA resets the counters
+    __threadfence();
+    if (atomicAdd(&g_sched_done[p.sched_slot], 1u) == gridDim.x - 1) {
+      g_sched_next[p.sched_slot] = 0;
+      g_sched_done[p.sched_slot] = 0;
+      __threadfence();
+    }
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -703,6 +758,7 @@ int cuda_fail(cudaError_t e) {
 }
 
 constexpr int kMaxDevices = 64;
+std::atomic<unsigned int> g_launch_seq{0};  // picks each launch's schedule counter pair
 std::mutex g_dev_mutex;
 int g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 unsupported
 int g_dev_sms[kMaxDevices];    // streaming multiprocessors per device
@@ -872,6 +928,7 @@ int prepare_launch(const void* q, const void* k, const void* v, void* o, float* 
   prm.n_splits = n_splits;
   prm.o_part = nullptr;
   prm.lse_part = nullptr;
+  prm.sched_slot = static_cast<int>(g_launch_seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
   // persistent: one CTA per SM (shared memory and TMEM allow no second), never more CTAs than items
   L->grid = static_cast<int>(items < g_dev_sms[L->dev] ? items : g_dev_sms[L->dev]);
   return ATTN_OK;
