@@ -357,11 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_s = [=](int t, uint32_t slot) {
       const uint64_t qd = sdesc_sw128(opaque(q_addr) + t * C::kTileBytes, 16, 1024);
       const uint64_t kd = sdesc_sw128(kv_addr + slot * C::kTileBytes, 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = ((kk / 4) * C::kColBlockBytes + (kk % 4) * 32) >> 4;
-        mma_bf16_ss_elect(tmem + t * BN, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
-      }
+      static_assert(C::kColBlockBytes == 16384, "K-step offsets of mma_bf16_ss_k8");
+      if constexpr (D == 128)
+        mma_bf16_ss_k8(tmem + t * BN, qd, kd, idesc_s);
+      else
+        mma_bf16_ss_k4(tmem + t * BN, qd, kd, idesc_s);
     };
     const uint32_t ones_addr = smem_u32(ones_s);
     auto issue_pv = [=](int t, uint32_t slot, bool accumulate) {
@@ -370,10 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t v_addr = opaque(kv_addr) + slot * C::kTileBytes;
       const uint64_t vd =
           sdesc_sw128(v_addr, C::kTensorRowSum ? ones_addr - v_addr : C::kColBlockBytes, 1024);
-#pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)
-        mma_bf16_ts_elect(tmem + 2 * BN + t * 128, tmem + t * BN + 64 + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
-                          (accumulate || kk > 0) ? 1u : 0u);
+      static_assert(BN == 128, "K steps of mma_bf16_ts_k8");
+      mma_bf16_ts_k8(tmem + 2 * BN + t * 128, tmem + t * BN + 64, vd, idesc_pv, accumulate ? 1u : 0u);
     };
     // wait for load number `n` of the K/V stream
     auto wait_kv = [&](uint32_t n) {
