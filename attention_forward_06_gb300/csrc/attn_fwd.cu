@@ -354,24 +354,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs the issue code (converged); one elected lane issues.
     // Operand descriptors are built once per tile; a K step moves the start
     // address field (bits 0-13, address >> 4) by a constant, never carrying out.
-    auto issue_s = [=](int t, uint32_t slot) {
+    // each issue ends with commits to up to two mbarriers (kNoBar: none)
+    auto issue_s = [=](int t, uint32_t slot, uint32_t bar0 = kNoBar, uint32_t bar1 = kNoBar) {
       const uint64_t qd = sdesc_sw128(opaque(q_addr) + t * C::kTileBytes, 16, 1024);
       const uint64_t kd = sdesc_sw128(kv_addr + slot * C::kTileBytes, 16, 1024);
       static_assert(C::kColBlockBytes == 16384, "K-step offsets of mma_bf16_ss_k8");
       if constexpr (D == 128)
-        mma_bf16_ss_k8(tmem + t * BN, qd, kd, idesc_s);
+        mma_bf16_ss_k8(tmem + t * BN, qd, kd, idesc_s, bar0, bar1);
       else
-        mma_bf16_ss_k4(tmem + t * BN, qd, kd, idesc_s);
+        mma_bf16_ss_k4(tmem + t * BN, qd, kd, idesc_s, bar0, bar1);
     };
     const uint32_t ones_addr = smem_u32(ones_s);
-    auto issue_pv = [=](int t, uint32_t slot, bool accumulate) {
+    auto issue_pv = [=](int t, uint32_t slot, bool accumulate, uint32_t bar0 = kNoBar, uint32_t bar1 = kNoBar) {
       // V is MN-major: the leading byte offset steps from one 64-column block of V to
       // the next; at D = 64 the second block is the ones block (the row-sum columns)
       const uint32_t v_addr = opaque(kv_addr) + slot * C::kTileBytes;
       const uint64_t vd =
           sdesc_sw128(v_addr, C::kTensorRowSum ? ones_addr - v_addr : C::kColBlockBytes, 1024);
       static_assert(BN == 128, "K steps of mma_bf16_ts_k8");
-      mma_bf16_ts_k8(tmem + 2 * BN + t * 128, tmem + t * BN + 64, vd, idesc_pv, accumulate ? 1u : 0u);
+      mma_bf16_ts_k8(tmem + 2 * BN + t * 128, tmem + t * BN + 64, vd, idesc_pv, accumulate ? 1u : 0u, bar0, bar1);
     };
     // wait for load number `n` of the K/V stream
     auto wait_kv = [&](uint32_t n) {
@@ -394,11 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kslot = kv_it % S;
       ++kv_it;
       tc_fence_after();
-      issue_s(0, kslot);
-      mma_commit_elect(&s_full[0]);
-      issue_s(1, kslot);
-      mma_commit_elect(&s_full[1]);
-      mma_commit_elect(&kv_empty[kslot]);
+      issue_s(0, kslot, smem_u32(&s_full[0]));
+      issue_s(1, kslot, smem_u32(&s_full[1]), smem_u32(&kv_empty[kslot]));
       if (n == 1) mma_commit_elect(&q_empty);
       for (int j = 0; j < n; ++j) {
         const uint32_t vslot = kv_it % S;
@@ -408,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = warp_wait(&p_full[0], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        issue_pv(0, vslot, j > 0);
-        if (j + 1 == n) mma_commit_elect(&o_final[0]);  // O_0 complete: its epilogue can start
+        // the last P.V of O_0 completes it: its epilogue can start
+        issue_pv(0, vslot, j > 0, j + 1 == n ? smem_u32(&o_final[0]) : kNoBar);
         const bool more = j + 1 < n;
         if (more) {
           kslot = kv_it % S;
@@ -417,20 +415,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++kv_it;
           if (!ok) break;
           tc_fence_after();
-          issue_s(0, kslot);
-          mma_commit_elect(&s_full[0]);
+          issue_s(0, kslot, smem_u32(&s_full[0]));
         }
         if (j == 0 && n_done > 0) ok = warp_wait(&o_empty[1], (n_done - 1) & 1, abort_v, kTimeoutNs);
         if (ok) ok = warp_wait(&p_full[1], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        issue_pv(1, vslot, j > 0);
-        if (j + 1 == n) mma_commit_elect(&o_final[1]);
-        mma_commit_elect(&kv_empty[vslot]);
+        issue_pv(1, vslot, j > 0, j + 1 == n ? smem_u32(&o_final[1]) : kNoBar, smem_u32(&kv_empty[vslot]));
         if (more) {
-          issue_s(1, kslot);
-          mma_commit_elect(&s_full[1]);
-          mma_commit_elect(&kv_empty[kslot]);
+          issue_s(1, kslot, smem_u32(&s_full[1]), smem_u32(&kv_empty[kslot]));
           if (j + 2 == n) mma_commit_elect(&q_empty);  // that was the item's last S
         }
         ++g;

@@ -335,33 +335,44 @@ __device__ __forceinline__ void mma_bf16_ts_elect(uint32_t d_tmem, uint32_t a_tm
       : "memory");
 }
 
+constexpr uint32_t kNoBar = 0xFFFFFFFFu;
+
 // A whole K loop in one issue: one elected lane issues the MMAs of all K steps
 // back to back (the first accumulates into D only if `accumulate`, the rest
-// always).  SS form: A and B descriptors advance by the given 16-byte units per
-// step.  STEPS is 4 or 8; offsets come from the shared-memory layout.
+// always), then commits them to up to two mbarriers (shared-memory addresses
+// bar0, bar1; kNoBar = none: address 0 is a valid shared-memory address).  SS form: A and B descriptors advance by the given
+// 16-byte units per step; offsets come from the shared-memory layout.
+#define ATTN_COMMITS(B0, B1)                                                                      \
+  "setp.ne.b32 c, %" #B0 ", -1;\n\tand.pred c, c, e;\n\t"                                      \
+  "@c tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%" #B0 "];\n\t"   \
+  "setp.ne.b32 c, %" #B1 ", -1;\n\tand.pred c, c, e;\n\t"                                      \
+  "@c tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%" #B1 "];\n\t"
 #define ATTN_MMA_SS_STEP(OA, OB)                                      \
   "add.s64 a, %1, " #OA ";\n\tadd.s64 b, %2, " #OB ";\n\t"            \
   "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-__device__ __forceinline__ void mma_bf16_ss_k8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+__device__ __forceinline__ void mma_bf16_ss_k8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t bar0 = kNoBar, uint32_t bar1 = kNoBar) {
   // K steps of 32 bytes within a 128-byte swizzle atom, then the next 64-column block (16384 B = 1024 units)
   asm volatile(
-      "{\n\t.reg .pred e, t, f;\n\t.reg .b64 a, b;\n\t"
+      "{\n\t.reg .pred e, t, f, c;\n\t.reg .b64 a, b;\n\t"
       "setp.eq.b32 t, 1, 1;\n\tsetp.eq.b32 f, 1, 0;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
       ATTN_MMA_SS_STEP(2, 2) ATTN_MMA_SS_STEP(4, 4) ATTN_MMA_SS_STEP(6, 6)
       ATTN_MMA_SS_STEP(1024, 1024) ATTN_MMA_SS_STEP(1026, 1026) ATTN_MMA_SS_STEP(1028, 1028)
-      ATTN_MMA_SS_STEP(1030, 1030) "}" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc)
+      ATTN_MMA_SS_STEP(1030, 1030) ATTN_COMMITS(4, 5) "}" ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc),
+      "r"(bar0), "r"(bar1)
       : "memory");
 }
-__device__ __forceinline__ void mma_bf16_ss_k4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+__device__ __forceinline__ void mma_bf16_ss_k4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t bar0 = kNoBar, uint32_t bar1 = kNoBar) {
   asm volatile(
-      "{\n\t.reg .pred e, t, f;\n\t.reg .b64 a, b;\n\t"
+      "{\n\t.reg .pred e, t, f, c;\n\t.reg .b64 a, b;\n\t"
       "setp.eq.b32 t, 1, 1;\n\tsetp.eq.b32 f, 1, 0;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
-      ATTN_MMA_SS_STEP(2, 2) ATTN_MMA_SS_STEP(4, 4) ATTN_MMA_SS_STEP(6, 6) "}" ::"r"(d_tmem), "l"(a_desc),
-      "l"(b_desc), "r"(idesc)
+      ATTN_MMA_SS_STEP(2, 2) ATTN_MMA_SS_STEP(4, 4) ATTN_MMA_SS_STEP(6, 6) ATTN_COMMITS(4, 5) "}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(bar0), "r"(bar1)
       : "memory");
 }
 #undef ATTN_MMA_SS_STEP
@@ -372,18 +383,19 @@ __device__ __forceinline__ void mma_bf16_ss_k4(uint32_t d_tmem, uint64_t a_desc,
   "add.u32 ta, %1, " #OA ";\n\tadd.s64 b, %2, " #OB ";\n\t"           \
   "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t"
 __device__ __forceinline__ void mma_bf16_ts_k8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate) {
+                                               uint32_t accumulate, uint32_t bar0 = kNoBar, uint32_t bar1 = kNoBar) {
   asm volatile(
-      "{\n\t.reg .pred e, t, f;\n\t.reg .b64 b;\n\t.reg .b32 ta;\n\t"
+      "{\n\t.reg .pred e, t, f, c;\n\t.reg .b64 b;\n\t.reg .b32 ta;\n\t"
       "setp.eq.b32 t, 1, 1;\n\tsetp.ne.b32 f, %4, 0;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, f;\n\t"
       ATTN_MMA_TS_STEP(8, 128) ATTN_MMA_TS_STEP(16, 256) ATTN_MMA_TS_STEP(24, 384) ATTN_MMA_TS_STEP(32, 512)
-      ATTN_MMA_TS_STEP(40, 640) ATTN_MMA_TS_STEP(48, 768) ATTN_MMA_TS_STEP(56, 896) "}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      ATTN_MMA_TS_STEP(40, 640) ATTN_MMA_TS_STEP(48, 768) ATTN_MMA_TS_STEP(56, 896) ATTN_COMMITS(5, 6) "}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(bar0), "r"(bar1)
       : "memory");
 }
 #undef ATTN_MMA_TS_STEP
+#undef ATTN_COMMITS
 
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
   asm volatile(
