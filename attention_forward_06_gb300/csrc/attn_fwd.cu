@@ -70,6 +70,7 @@ constexpr int ROWS_PER_ITEM = QTILES * BM;
 constexpr int kThreads = 384;    // 3 warpgroups
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kStoreWarp = 11;  // O stores of the epilogue
 constexpr uint32_t kRegsLaunch = 168;   // 65536 / 384, what ptxas assigns under the launch bounds
 constexpr uint32_t kRegsSoftmax = 224;  // warpgroups 0 and 1
 constexpr uint32_t kRegsOther = 56;     // warpgroup 2 (producer, issuer, two idle warps)
@@ -180,7 +181,7 @@ constexpr int kSchedSlots = 64;
 __device__ int g_sched_next[kSchedSlots];
 __device__ unsigned int g_sched_done[kSchedSlots];
 constexpr int kSeqSlots = 4;  // depth of the shared-memory ring through which the producer publishes items
-constexpr int kSeqConsumers = 9;  // warps reading the ring: eight softmax warps and the issuer
+constexpr int kSeqConsumers = 10;  // warps reading the ring: eight softmax warps, the issuer, the store warp
 
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ones_s = st_s + C::kStageBufs * C::kStageBytes;  // D = 64: the ones block of the row-sum columns
   __shared__ uint64_t kv_full[S], kv_empty[S];
   __shared__ uint64_t q_full, q_empty, s_full[QTILES], p_full[QTILES], o_final[QTILES], o_empty[QTILES];
-  __shared__ uint64_t stage_rel[QTILES], mma_drain;
+  __shared__ uint64_t stage_full[QTILES], stage_rel[QTILES], mma_drain;
   __shared__ uint64_t seq_full[kSeqSlots], seq_empty[kSeqSlots];
   __shared__ int item_seq[kSeqSlots];  // the CTA's k-th item at slot k % kSeqSlots (-1: no more)
   __shared__ uint32_t tmem_base_slot;
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&p_full[t], 4 * 32);
       mbar_init(&o_empty[t], 4 * 32);
       mbar_init(&o_final[t], 1);
+      mbar_init(&stage_full[t], 4 * 32);
       mbar_init(&stage_rel[t], 1);
     }
     mbar_init(&mma_drain, 1);
@@ -322,6 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             it.bh);
       ++q_issued;
       for (int i = 0; i < 2 * it.n_tiles; ++i) {  // K_j is load 2j, V_j is load 2j+1
+        if (k == 0 && i == 2) {
+          // all CTAs start at once: let the first item's Q and K_0 land before streaming
+          // more, so they are not queued behind the rest of the start-up burst in DRAM
+          ok = warp_wait(&q_full, 0, abort_v, kTimeoutNs) && warp_wait(&kv_full[0], 0, abort_v, kTimeoutNs);
+          if (!ok) break;
+        }
         const uint32_t slot = kv_it % S;
         const uint32_t use = kv_it / S;
         if (use > 0) {
@@ -435,6 +443,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every MMA issued above has completed before TMEM can be freed
     mma_commit_elect(&mma_drain);
     warp_wait(&mma_drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
+   } else if (warp == kStoreWarp) {
+    // ------------------------------------------------------------ O stores
+    // Once a Q tile's epilogue has staged O (stage_full), one TMA store per 64
+    // columns writes it out; the staging buffer is handed back (stage_rel) when the
+    // stores have read it.  The softmax warps never wait for a store.
+    uint32_t e_seen[QTILES] = {0, 0};
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      int x;
+      ok = next_item(k, x);
+      if (!ok || x < 0) break;
+      if constexpr (!SPLIT) {  // split-key partials are written by the softmax warps directly
+        const Item it = item_at<SPLIT>(p, x);
+        if (it.n_tiles == 0) continue;
+        for (int t = 0; t < QTILES && ok; ++t) {
+          ok = warp_wait(&stage_full[t], e_seen[t] & 1, abort_v, kTimeoutNs);
+          if (!ok) break;
+          ++e_seen[t];
+          uint8_t* stage = st_s + ((C::kStageBufs == 1) ? 0 : t) * C::kStageBytes;
+#pragma unroll
+          for (int cb = 0; cb < D / 64; ++cb)
+            tma_store_3d_elect(&to, stage + cb * (BM * 128), cb * 64, it.q0 + t * BM, it.bh);
+          bulk_commit_group_elect();
+          bulk_wait_group_read0();  // the staging tile has been read: hand it on
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&stage_rel[t]);
+        }
+      }
+    }
+    if (!ok && lane == 0) record_abort(abort_v, kSiteEpilogue);
+    bulk_wait_group0();  // every store has landed before the CTA exits
    }
   } else {
     // ------------------------------------------------------------ softmax (+ rescale, epilogue)
@@ -706,20 +745,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           *dst = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      fence_proxy_async_smem();
-      named_barrier_sync(1 + t, 128);  // the whole tile is staged
-      if (quarter == 0) {
-#pragma unroll
-        for (int cb = 0; cb < D / 64; ++cb)
-          tma_store_3d_elect(&to, stage + cb * (BM * 128), cb * 64, it.q0 + t * BM, it.bh);
-        bulk_commit_group_elect();
-        bulk_wait_group_read0();  // the staging tile has been read: hand it on
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&stage_rel[t]);
-      }
+      fence_proxy_async_smem();  // this thread's staged row is visible to the TMA store
+      mbar_arrive(&stage_full[t]);  // the store warp writes the tile out
       if (live) *lrow = any_key ? (m + lg2_approx(l_exact)) * 0.69314718055994531f : -INFINITY;
     }
-    if (quarter == 0) bulk_wait_group0();  // this warp's TMA stores have landed
   }
 
   tc_fence_before();
