@@ -32,6 +32,13 @@
  *   - a row with no allowed key has O = 0 and LSE = -inf.
  *   - inputs arrive as raw bf16 bit patterns and are widened exactly; scale is
  *     the fp32 value the GPU receives, widened exactly to fp64.
+ *   - block mask (attn_ref_fwd_masked): the keys a row may attend to are further
+ *     restricted to the key blocks its query block's bit-packed mask row marks
+ *     (page "AdaSplash-2: Faster Differentiable Sparse Attention", technical
+ *     summary section 2, bit-packed block masking: one bit per (query block,
+ *     key block), 32 blocks per 32-bit word).  Layout
+ *     mask[b][hm][i / block_q][w], hm = 0 when one mask serves every head else
+ *     h; bit (kb % 32) of word kb / 32 marks key block kb = j / block_k.
  *
  * Build: gcc -O2 -fopenmp -shared -fPIC attn_ref.c -o libattn_ref.so -lm
  * Portable C99: no intrinsics, no architecture flags (runs on x86_64 and aarch64).
@@ -61,38 +68,52 @@ static int64_t allowed_keys(int64_t i, int64_t Sq, int64_t Sk, int causal) {
     return last < 0 ? 0 : last + 1;
 }
 
+/* Whether key j passes the row's block-mask words (NULL: no block mask). */
+static int block_visible(const uint32_t* mask_row, int64_t j, int block_k) {
+    int64_t kb;
+    if (!mask_row) return 1;
+    kb = j / block_k;
+    return (int)((mask_row[kb / 32] >> (kb % 32)) & 1u);
+}
+
 /*
  * One query row.  s (scratch) and p (optional output) hold at least Sk doubles.
- * q_row: D bf16; kh, vh: the kv head's [Sk][D] bf16.  Writes o_row[D] and *lse.
+ * q_row: D bf16; kh, vh: the kv head's [Sk][D] bf16; mask_row: the row's block-mask
+ * words or NULL.  Writes o_row[D] and *lse.
  */
 static void ref_row(const uint16_t* q_row, const uint16_t* kh, const uint16_t* vh,
                     int64_t i, int64_t Sq, int64_t Sk, int64_t D, int causal, double scale,
+                    const uint32_t* mask_row, int block_k,
                     double* s, double* p, double* o_row, double* lse) {
     int64_t n = allowed_keys(i, Sq, Sk, causal);
-    int64_t j, d;
-    double m, l;
+    int64_t j, d, seen = 0;
+    double m = -INFINITY, l;
 
     for (d = 0; d < D; ++d) o_row[d] = 0.0;
     if (p) for (j = 0; j < Sk; ++j) p[j] = 0.0;
-    if (n == 0) {
-        *lse = -INFINITY;
-        return;
-    }
-    /* logits of the allowed keys */
+    /* logits of the allowed keys, and their maximum */
     for (j = 0; j < n; ++j) {
         double acc = 0.0;
+        if (!block_visible(mask_row, j, block_k)) continue;
         for (d = 0; d < D; ++d)
             acc += bf16_bits_to_f64(q_row[d]) * bf16_bits_to_f64(kh[j * D + d]);
         s[j] = scale * acc;
+        if (seen == 0 || s[j] > m) m = s[j];
+        ++seen;
     }
-    /* row maximum and normaliser */
-    m = s[0];
-    for (j = 1; j < n; ++j) if (s[j] > m) m = s[j];
+    if (seen == 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    /* normaliser */
     l = 0.0;
-    for (j = 0; j < n; ++j) l += exp(s[j] - m);
+    for (j = 0; j < n; ++j)
+        if (block_visible(mask_row, j, block_k)) l += exp(s[j] - m);
     /* probabilities, then the weighted sum of value rows */
     for (j = 0; j < n; ++j) {
-        double pj = exp(s[j] - m) / l;
+        double pj;
+        if (!block_visible(mask_row, j, block_k)) continue;
+        pj = exp(s[j] - m) / l;
         if (p) p[j] = pj;
         for (d = 0; d < D; ++d) o_row[d] += pj * bf16_bits_to_f64(vh[j * D + d]);
     }
@@ -106,25 +127,21 @@ static int check_args(int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal)
     return 0;
 }
 
-/*
- * Full or row-subset forward.
- *   rows == NULL: every row; o is [B][Hq][Sq][D], lse is [B][Hq][Sq].
- *   rows != NULL: nrows flat row ids r = (b*Hq + h)*Sq + i; o is [nrows][D],
- *                 lse is [nrows] (compact, in the order given).
- * Returns 0 on success, 1 on bad arguments, 2 on allocation failure.
- */
-int attn_ref_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                 double* o, double* lse,
-                 int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
-                 const int64_t* rows, int64_t nrows) {
+static int fwd_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, double* o, double* lse,
+                    int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                    const uint32_t* mask, int mask_heads, int block_q, int block_k,
+                    const int64_t* rows, int64_t nrows) {
     const int64_t G = (Hkv > 0) ? (int64_t)Hq / Hkv : 1;
     const int64_t total = (int64_t)B * Hq * Sq;
     const int64_t count = rows ? nrows : total;
     const double scale64 = (double)scale;
+    const int64_t qblocks = (mask && block_q > 0) ? ((int64_t)Sq + block_q - 1) / block_q : 0;
+    const int64_t words = (mask && block_k > 0) ? (((int64_t)Sk + block_k - 1) / block_k + 31) / 32 : 0;
     int failed = 0;
     int64_t t;
 
     if (check_args(B, Hq, Hkv, Sq, Sk, D, causal)) return 1;
+    if (mask && (block_q <= 0 || block_k <= 0 || (mask_heads != 1 && mask_heads != Hq))) return 1;
     if (rows) {
         for (t = 0; t < nrows; ++t)
             if (rows[t] < 0 || rows[t] >= total) return 1;
@@ -139,13 +156,48 @@ int attn_ref_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         const int64_t kvh = h / G;
         const uint16_t* kh = k + ((b * Hkv + kvh) * (int64_t)Sk) * D;
         const uint16_t* vh = v + ((b * Hkv + kvh) * (int64_t)Sk) * D;
-        double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+        const uint32_t* mrow = NULL;
+        double* s;
+        if (mask) {
+            const int64_t hm = (mask_heads == 1) ? 0 : h;
+            mrow = mask + ((b * mask_heads + hm) * qblocks + i / block_q) * words;
+        }
+        s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
         if (!s) { failed |= 1; continue; }
-        ref_row(q + r * D, kh, vh, i, Sq, Sk, D, causal, scale64, s, NULL,
+        ref_row(q + r * D, kh, vh, i, Sq, Sk, D, causal, scale64, mrow, block_k, s, NULL,
                 o + t * D, lse + t);
         free(s);
     }
     return failed ? 2 : 0;
+}
+
+/*
+ * Full or row-subset forward.
+ *   rows == NULL: every row; o is [B][Hq][Sq][D], lse is [B][Hq][Sq].
+ *   rows != NULL: nrows flat row ids r = (b*Hq + h)*Sq + i; o is [nrows][D],
+ *                 lse is [nrows] (compact, in the order given).
+ * Returns 0 on success, 1 on bad arguments, 2 on allocation failure.
+ */
+int attn_ref_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                 double* o, double* lse,
+                 int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                 const int64_t* rows, int64_t nrows) {
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, NULL, 1, 1, 1, rows, nrows);
+}
+
+/*
+ * The same with a bit-packed block mask (layout in the header comment; blocks of
+ * block_q query rows by block_k keys; mask_heads 1 or Hq).  A row whose allowed
+ * keys all fall in unmarked blocks has O = 0 and LSE = -inf.
+ */
+int attn_ref_fwd_masked(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        double* o, double* lse,
+                        int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                        const uint32_t* mask, int mask_heads, int block_q, int block_k,
+                        const int64_t* rows, int64_t nrows) {
+    if (!mask) return 1;
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, mask, mask_heads, block_q, block_k,
+                    rows, nrows);
 }
 
 /*
@@ -162,7 +214,7 @@ int attn_ref_probs(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
     if (!s) return 2;
     for (i = 0; i < Sq; ++i)
-        ref_row(q + i * D, k, v, i, Sq, Sk, D, causal, (double)scale, s,
+        ref_row(q + i * D, k, v, i, Sq, Sk, D, causal, (double)scale, NULL, 1, s,
                 p + i * (int64_t)Sk, o + i * D, lse + i);
     free(s);
     return 0;

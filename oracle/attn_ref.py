@@ -56,6 +56,9 @@ def _load():
             lib.attn_ref_fwd.restype = ctypes.c_int
             lib.attn_ref_fwd.argtypes = [u16p, u16p, u16p, f64p, f64p] + [ctypes.c_int] * 7 + [
                 ctypes.c_float, i64p, ctypes.c_int64]
+            lib.attn_ref_fwd_masked.restype = ctypes.c_int
+            lib.attn_ref_fwd_masked.argtypes = [u16p, u16p, u16p, f64p, f64p] + [ctypes.c_int] * 7 + [
+                ctypes.c_float, ctypes.POINTER(ctypes.c_uint32)] + [ctypes.c_int] * 3 + [i64p, ctypes.c_int64]
             lib.attn_ref_probs.restype = ctypes.c_int
             lib.attn_ref_probs.argtypes = [u16p, u16p, u16p, f64p, f64p, f64p] + [ctypes.c_int] * 4 + [
                 ctypes.c_float]
@@ -81,12 +84,15 @@ def num_threads() -> int:
     return int(_load().attn_ref_num_threads())
 
 
-def attention(q, k, v, causal: int, scale: float, rows=None):
+def attention(q, k, v, causal: int, scale: float, rows=None, block_mask=None, block=(128, 128)):
     """Exact attention forward in fp64.
 
     Returns ``(o, lse)``.  With ``rows=None``: ``o [B,Hq,Sq,D]``, ``lse [B,Hq,Sq]``.
     With ``rows`` (flat ids ``(b*Hq + h)*Sq + i``): ``o [len(rows), D]``, ``lse [len(rows)]``.
     ``scale`` is rounded to fp32 first: the oracle uses the value the GPU receives.
+    ``block_mask`` (optional): uint32 ``[B, 1 or Hq, ceil(Sq/bq), ceil(ceil(Sk/bk)/32)]``, bit ``kb % 32``
+    of word ``kb // 32`` marking key block ``kb`` visible to a query block (``block = (bq, bk)``);
+    it restricts the keys on top of ``causal`` (page "AdaSplash-2", technical summary section 2).
     """
     q, k, v = _u16(q), _u16(k), _u16(v)
     if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
@@ -104,11 +110,24 @@ def attention(q, k, v, causal: int, scale: float, rows=None):
         nrows = rows_arr.size
         o = np.empty((nrows, D), np.float64)
         lse = np.empty((nrows,), np.float64)
-    rc = _load().attn_ref_fwd(
-        _ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
-        _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
-        B, Hq, Hkv, Sq, Sk, D, int(causal), float(np.float32(scale)),
-        _ptr(rows_arr, ctypes.c_int64) if rows_arr is not None else None, nrows)
+    rows_ptr = _ptr(rows_arr, ctypes.c_int64) if rows_arr is not None else None
+    if block_mask is None:
+        rc = _load().attn_ref_fwd(
+            _ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
+            _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+            B, Hq, Hkv, Sq, Sk, D, int(causal), float(np.float32(scale)), rows_ptr, nrows)
+    else:
+        bq, bk = block
+        mask = np.ascontiguousarray(block_mask, dtype=np.uint32)
+        words = (-(-Sk // bk) + 31) // 32
+        if mask.ndim != 4 or mask.shape[0] != B or mask.shape[1] not in (1, Hq) or \
+                mask.shape[2] != -(-Sq // bq) or mask.shape[3] != words:
+            raise ValueError(f"block mask shape {mask.shape} does not fit B={B} Hq={Hq} Sq={Sq} Sk={Sk}")
+        rc = _load().attn_ref_fwd_masked(
+            _ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
+            _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+            B, Hq, Hkv, Sq, Sk, D, int(causal), float(np.float32(scale)),
+            _ptr(mask, ctypes.c_uint32), int(mask.shape[1]), int(bq), int(bk), rows_ptr, nrows)
     if rc != 0:
         raise ValueError(f"attn_ref_fwd failed with status {rc}")
     return o, lse
