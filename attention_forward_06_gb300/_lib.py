@@ -28,6 +28,8 @@ SIGNATURES = {
         "attn_fwd_splitkv_workspace_size": (ctypes.c_size_t, [_c_int] * 5),
         "attn_fwd_splitkv_suggest": (_c_int, [_c_int] * 6),
         "attn_fwd_splitkv_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _vp]),
+        "attn_fwd_blocksparse": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp, _c_int, _vp]),
+        "attn_fwd_block_mask_words": (ctypes.c_size_t, [_c_int] * 4),
     },
     "attn_probe": {
         "attn_probe_mma_ss": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _vp, _vp]),

@@ -122,6 +122,12 @@ struct Params {
   float* o_part;    // [n_splits][BH][Sq][D]
   float* lse_part;  // [n_splits][BH][Sq]
   int sched_slot;   // counter pair of the dynamic schedule used by this launch
+  // block-sparse mode: bit-packed mask [B][mask_heads][n_qtiles][mask_words], one bit per
+  // (128-row query block, 128-key block), bit kb % 32 of word kb / 32
+  const uint32_t* mask;
+  int mask_heads;  // 1 (one mask for every head) or Hq
+  int mask_words;  // words per mask row: ceil(ceil(Sk / 128) / 32)
+  int n_qtiles;    // ceil(Sq / 128)
 };
 
 struct Item {
@@ -135,7 +141,7 @@ struct Item {
 
 // Item x of the heaviest-first list: query block from the last, then (split-key
 // mode) the key range, heads fastest.
-template <bool SPLIT>
+template <bool SPLIT, bool SPARSE = false>
 __device__ __forceinline__ Item item_at(const Params& p, int x) {
   Item it;
   int qb, r;
@@ -165,9 +171,47 @@ __device__ __forceinline__ Item item_at(const Params& p, int x) {
     it.n_tiles = static_cast<int>(static_cast<int64_t>(it.split + 1) * n_full / p.n_splits) - it.j0;
   } else {
     it.j0 = 0;
-    it.n_tiles = n_full;
+    it.n_tiles = n_full;  // block-sparse mode: the causal bound; the producer counts the marked tiles
   }
   return it;
+}
+
+// Block-sparse mode: the two mask rows of an item (its Q tiles' query blocks; a Q
+// tile past the last query block has none), word w of their union clipped to the
+// item's causal key-tile bound n_full, and that tile's own bits.
+struct MaskRows {
+  const uint32_t* r0;  // Q tile 0's row
+  const uint32_t* r1;  // Q tile 1's row, or nullptr
+};
+
+__device__ __forceinline__ MaskRows mask_rows(const Params& p, const Item& it) {
+  const int b = it.bh / p.Hq;
+  const int hm = p.mask_heads == 1 ? 0 : it.bh % p.Hq;
+  const int qt = it.q0 / BM;
+  const uint32_t* base = p.mask + (static_cast<int64_t>(b) * p.mask_heads + hm) * p.n_qtiles * p.mask_words;
+  MaskRows m;
+  m.r0 = base + static_cast<int64_t>(qt) * p.mask_words;
+  m.r1 = qt + 1 < p.n_qtiles ? m.r0 + p.mask_words : nullptr;
+  return m;
+}
+
+// bits of word w kept by a key-tile bound n (tiles 0 .. n-1)
+__device__ __forceinline__ uint32_t bound_bits(int w, int n) {
+  const int left = n - 32 * w;
+  return left >= 32 ? 0xFFFFFFFFu : (left <= 0 ? 0u : ((1u << left) - 1u));
+}
+
+__device__ __forceinline__ uint32_t union_word(const MaskRows& m, int w, int n) {
+  const uint32_t u = __ldg(m.r0 + w) | (m.r1 ? __ldg(m.r1 + w) : 0u);
+  return u & bound_bits(w, n);
+}
+
+// number of key tiles the item visits: the marked tiles within its causal bound
+__device__ __forceinline__ int sparse_tiles(const Params& p, const Item& it) {
+  const MaskRows m = mask_rows(p, it);
+  int n = 0;
+  for (int w = 0; w * 32 < it.n_tiles; ++w) n += __popc(union_word(m, w, it.n_tiles));
+  return n;
 }
 
 __device__ int g_status;  // sticky: 0 = fine, else the site of the first wait that ran out
@@ -200,7 +244,7 @@ __device__ __forceinline__ void record_abort(volatile uint32_t* abort_flag, int 
   atomicCAS(&g_status, 0, site);
 }
 
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -218,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t stage_full[QTILES], stage_rel[QTILES], mma_drain;
   __shared__ uint64_t seq_full[kSeqSlots], seq_empty[kSeqSlots];
   __shared__ int item_seq[kSeqSlots];  // the CTA's k-th item at slot k % kSeqSlots (-1: no more)
+  __shared__ int item_ntiles[kSeqSlots];  // block-sparse mode: its marked key tiles (counted by the producer)
   __shared__ uint32_t tmem_base_slot;
   __shared__ uint32_t abort_flag;
 
@@ -264,9 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_slot;
   volatile uint32_t* abort_v = &abort_flag;
   // k-th item of this CTA as published by the producer (-1: no more); false when a wait gave up
-  auto next_item = [&](int k, int& x) {
+  auto next_item = [&](int k, int& x, int* ntiles = nullptr) {
     if (!warp_wait(&seq_full[k % kSeqSlots], (k / kSeqSlots) & 1, abort_v, kTimeoutNs)) return false;
     x = *reinterpret_cast<volatile int*>(&item_seq[k % kSeqSlots]);
+    if (ntiles) *ntiles = *reinterpret_cast<volatile int*>(&item_ntiles[k % kSeqSlots]);
     __syncwarp();
     if (lane == 0) mbar_arrive(&seq_empty[k % kSeqSlots]);
     return true;
@@ -293,13 +339,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = warp_wait(&seq_empty[k % kSeqSlots], (k / kSeqSlots - 1) & 1, abort_v, kTimeoutNs);
         if (!ok) break;
       }
+      int n_marked = 0;  // block-sparse mode: the item's marked key tiles
+      if constexpr (SPARSE) {
+        if (more) n_marked = sparse_tiles(p, item_at<SPLIT, SPARSE>(p, x));
+      }
       if (lane == 0) {
         item_seq[k % kSeqSlots] = more ? x : -1;
+        if constexpr (SPARSE) item_ntiles[k % kSeqSlots] = n_marked;
         mbar_arrive(&seq_full[k % kSeqSlots]);
       }
       __syncwarp();
       if (!more) break;
-      const Item it = item_at<SPLIT>(p, x);
+      const Item it = item_at<SPLIT, SPARSE>(p, x);
+      const int n_tiles = SPARSE ? n_marked : it.n_tiles;
       // The next item is claimed once this item's loads are all issued (about two
       // key tiles before its end), so items are handed out in the order CTAs free up.
       auto claim = [&]() {
@@ -307,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) claimed = atomicAdd(&g_sched_next[p.sched_slot], 1);
         return static_cast<int>(gridDim.x) + __shfl_sync(0xffffffffu, claimed, 0);
       };
-      if (it.n_tiles == 0) {
+      if (n_tiles == 0) {
         x = claim();
         continue;
       }
@@ -323,7 +375,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d_elect(q_s + t * C::kTileBytes + cb * C::kColBlockBytes, &tq, &q_full, cb * 64, it.q0 + t * BM,
                             it.bh);
       ++q_issued;
-      for (int i = 0; i < 2 * it.n_tiles; ++i) {  // K_j is load 2j, V_j is load 2j+1
+      // block-sparse mode: the marked key tiles in order (find-first-set over the union words)
+      MaskRows mrows{};
+      int mw = 0;
+      uint32_t mcur = 0;
+      int kb = 0;
+      if constexpr (SPARSE) {
+        mrows = mask_rows(p, it);
+        mcur = union_word(mrows, 0, it.n_tiles);
+      }
+      for (int i = 0; i < 2 * n_tiles; ++i) {  // K_j is load 2j, V_j is load 2j+1
         if (k == 0 && i == 2) {
           // all CTAs start at once: let the first item's Q and K_0 land before streaming
           // more, so they are not queued behind the rest of the start-up burst in DRAM
@@ -337,11 +398,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         const CUtensorMap* map = (i & 1) ? &tv : &tk;
+        if constexpr (SPARSE) {
+          if (!(i & 1)) {  // the next marked tile (the item has n_tiles of them)
+            const int mw_end = (it.n_tiles + 31) / 32;  // bounded even if the mask changed under the call
+            while (mcur == 0 && mw + 1 < mw_end) mcur = union_word(mrows, ++mw, it.n_tiles);
+            kb = mcur ? 32 * mw + __ffs(mcur) - 1 : 0;
+            mcur &= mcur - 1;
+          }
+        } else {
+          kb = it.j0 + (i >> 1);
+        }
         mbar_arrive_expect_tx_elect(&kv_full[slot], C::kTileBytes);
 #pragma unroll
         for (int cb = 0; cb < D / 64; ++cb)
           tma_load_3d_elect(kv_s + slot * C::kTileBytes + cb * C::kColBlockBytes, map, &kv_full[slot], cb * 64,
-                            (it.j0 + (i >> 1)) * BN, it.kv_z);
+                            kb * BN, it.kv_z);
         ++kv_it;
       }
       if (ok) x = claim();
@@ -391,11 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n_done = 0;  // items with key tiles processed
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      int x;
-      ok = next_item(k, x);
+      int x, n_marked = 0;
+      ok = next_item(k, x, SPARSE ? &n_marked : nullptr);
       if (!ok || x < 0) break;
-      const Item it = item_at<SPLIT>(p, x);
-      const int n = it.n_tiles;
+      const int n = SPARSE ? n_marked : item_at<SPLIT>(p, x).n_tiles;
       if (n == 0) continue;
       ok = warp_wait(&q_full, n_done & 1, abort_v, kTimeoutNs);
       if (ok) ok = wait_kv(kv_it);
@@ -451,12 +521,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t e_seen[QTILES] = {0, 0};
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      int x;
-      ok = next_item(k, x);
+      int x, n_marked = 0;
+      ok = next_item(k, x, SPARSE ? &n_marked : nullptr);
       if (!ok || x < 0) break;
       if constexpr (!SPLIT) {  // split-key partials are written by the softmax warps directly
-        const Item it = item_at<SPLIT>(p, x);
-        if (it.n_tiles == 0) continue;
+        const Item it = item_at<SPLIT, SPARSE>(p, x);
+        if ((SPARSE ? n_marked : it.n_tiles) == 0) continue;
         for (int t = 0; t < QTILES && ok; ++t) {
           ok = warp_wait(&stage_full[t], e_seen[t] & 1, abort_v, kTimeoutNs);
           if (!ok) break;
@@ -489,21 +559,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
-      int x;
-      ok = next_item(k, x);
+      int x, n_marked = 0;
+      ok = next_item(k, x, SPARSE ? &n_marked : nullptr);
       if (!ok) {
         if (lane == 0) record_abort(abort_v, kSiteSoftmax);
         break;
       }
       if (x < 0) break;
-      const Item it = item_at<SPLIT>(p, x);
+      const Item it = item_at<SPLIT, SPARSE>(p, x);
+      const int n_tiles = SPARSE ? n_marked : it.n_tiles;  // key tiles the item visits
       const int row = it.q0 + t * BM + quarter * 32 + lane;  // global query row
       const bool live = row < p.Sq;
       __nv_bfloat16* orow = p.o + (static_cast<int64_t>(it.bh) * p.Sq + row) * D;
       float* lrow = p.lse + static_cast<int64_t>(it.bh) * p.Sq + row;
       // split-key mode: this item's partial result rows
       const int64_t prow = (static_cast<int64_t>(it.split) * p.BH + it.bh) * p.Sq + row;
-      if (it.n_tiles == 0) {  // no key is visible to any row of this item (or its key range is empty)
+      if (n_tiles == 0) {  // no key is visible to any row of this item (or its key range is empty)
         if (live) {
           if (SPLIT) {
             float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
@@ -530,15 +601,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       float l = 0.0f;        // sum of the bf16-rounded P the tensor cores use (normalises O)
       float l_exact = 0.0f;  // sum of the fp32 P (gives LSE)
 
-      for (int j = 0; j < it.n_tiles; ++j, ++g) {
+      // block-sparse mode: walk the same marked tiles as the producer; a tile that only
+      // the other Q tile's query block marks is wholly masked for this one
+      MaskRows mrows{};
+      int mw = 0;
+      uint32_t mcur = 0, mown = 0;
+      if constexpr (SPARSE) {
+        mrows = mask_rows(p, it);
+        mcur = union_word(mrows, 0, it.n_tiles);
+        mown = t == 0 ? __ldg(mrows.r0) : (mrows.r1 ? __ldg(mrows.r1) : 0u);
+      }
+      for (int j = 0; j < n_tiles; ++j, ++g) {
         ok = warp_wait(&s_full[t], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
         uint32_t r[128];
         tmem_ld128_wait(s_tmem, r);
-        const int jg = it.j0 + j;            // key tile index within the head
-        const bool masked = jg * BN + BN - 1 > lim_tile;  // tile straddles the diagonal or the end of K
-        const int kmax = lim - jg * BN;
+        int jg = it.j0 + j;  // key tile index within the head
+        bool own = true;     // block-sparse mode: this Q tile's query block marks the tile
+        if constexpr (SPARSE) {
+          const int mw_end = (it.n_tiles + 31) / 32;
+          while (mcur == 0 && mw + 1 < mw_end) {
+            mcur = union_word(mrows, ++mw, it.n_tiles);
+            mown = t == 0 ? __ldg(mrows.r0 + mw) : (mrows.r1 ? __ldg(mrows.r1 + mw) : 0u);
+          }
+          const int bit = mcur ? __ffs(mcur) - 1 : 0;
+          jg = 32 * mw + bit;
+          own = (mown >> bit) & 1u;
+          mcur &= mcur - 1;
+        }
+        // the tile is unmarked for this Q tile, or straddles the diagonal or the end of K
+        const bool masked = !own || jg * BN + BN - 1 > lim_tile;
+        const int kmax = own ? lim - jg * BN : -1;
         if (masked) {
 #pragma unroll
           for (int i = 0; i < 128; ++i) r[i] = (i > kmax) ? __float_as_uint(-INFINITY) : r[i];
@@ -801,17 +895,18 @@ int prepare_device(int dev) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e);
   g_dev_sms[dev] = sms;
-  e = cudaFuncSetAttribute(attn_fwd_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<128>::kSmemBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_fwd_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<128>::kSmemBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_fwd_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<64>::kSmemBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_fwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<64>::kSmemBytes);
+  const void* k128[] = {reinterpret_cast<const void*>(attn_fwd_kernel<128, false, false>),
+                        reinterpret_cast<const void*>(attn_fwd_kernel<128, true, false>),
+                        reinterpret_cast<const void*>(attn_fwd_kernel<128, false, true>)};
+  const void* k64[] = {reinterpret_cast<const void*>(attn_fwd_kernel<64, false, false>),
+                       reinterpret_cast<const void*>(attn_fwd_kernel<64, true, false>),
+                       reinterpret_cast<const void*>(attn_fwd_kernel<64, false, true>)};
+  for (const void* f : k128)
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<128>::kSmemBytes);
+  for (const void* f : k64)
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<64>::kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e);
   if (!attn_host::encode_tiled_fn()) return ATTN_ERR_TENSOR_MAP;
   g_dev_state[dev] = 1;
@@ -949,14 +1044,19 @@ int prepare_launch(const void* q, const void* k, const void* v, void* o, float* 
   prm.o_part = nullptr;
   prm.lse_part = nullptr;
   prm.sched_slot = static_cast<int>(g_launch_seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+  prm.mask = nullptr;
+  prm.mask_heads = 1;
+  prm.mask_words = 0;
+  prm.n_qtiles = static_cast<int>((Sq + BM - 1) / BM);
   // persistent: one CTA per SM (shared memory and TMEM allow no second), never more CTAs than items
   L->grid = static_cast<int>(items < g_dev_sms[L->dev] ? items : g_dev_sms[L->dev]);
   return ATTN_OK;
 }
 
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool SPARSE = false>
 int launch(const Launch& L, cudaStream_t stream) {
-  attn_fwd_kernel<D, SPLIT><<<L.grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(L.tq, L.tk, L.tv, L.to, L.prm);
+  attn_fwd_kernel<D, SPLIT, SPARSE><<<L.grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(L.tq, L.tk, L.tv, L.to,
+                                                                                     L.prm);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -1058,6 +1158,37 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
       overlaps(workspace, need, o, qb) || overlaps(workspace, need, lse, static_cast<size_t>(rows) * 4))
     return ATTN_ERR_INVALID_ARG;
   return run_splitkv(L, workspace, rows, D, stream);
+}
+
+size_t attn_fwd_block_mask_words(int B, int mask_heads, int Sq, int Sk) {
+  if (B < 0 || mask_heads < 1 || Sq < 0 || Sk < 0) return 0;
+  const int64_t kblocks = (static_cast<int64_t>(Sk) + BN - 1) / BN;
+  const int64_t qblocks = (static_cast<int64_t>(Sq) + BM - 1) / BM;
+  return static_cast<size_t>(B) * mask_heads * qblocks * ((kblocks + 31) / 32);
+}
+
+int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                         int Sq, int Sk, int D, int causal, float scale, const uint32_t* block_mask, int mask_heads,
+                         cudaStream_t stream) {
+  // the mask's own checks (host only, before any CUDA call), then the common ones
+  if (Hq < 1 || (mask_heads != 1 && mask_heads != Hq)) return ATTN_ERR_INVALID_ARG;
+  const size_t words = (B > 0 && Sq > 0 && Sk > 0) ? attn_fwd_block_mask_words(B, mask_heads, Sq, Sk) : 0;
+  if (words > 0) {
+    if (!block_mask) return ATTN_ERR_NULL_PTR;
+    if ((reinterpret_cast<uintptr_t>(block_mask) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+    if (D > 0) {
+      const size_t mb = words * 4;
+      const size_t qb = static_cast<size_t>(B) * Hq * Sq * D * 2, lb = static_cast<size_t>(B) * Hq * Sq * 4;
+      if (overlaps(block_mask, mb, o, qb) || overlaps(block_mask, mb, lse, lb)) return ATTN_ERR_INVALID_ARG;
+    }
+  }
+  Launch L;
+  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, 1, &L);
+  if (st != ATTN_OK || L.empty) return st;
+  L.prm.mask = block_mask;
+  L.prm.mask_heads = mask_heads;
+  L.prm.mask_words = static_cast<int>(((static_cast<int64_t>(Sk) + BN - 1) / BN + 31) / 32);
+  return D == 128 ? launch<128, false, true>(L, stream) : launch<64, false, true>(L, stream);
 }
 
 int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,

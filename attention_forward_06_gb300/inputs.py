@@ -101,3 +101,19 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
 def from_values(values, dtype=torch.bfloat16) -> torch.Tensor:
     """A CPU bf16 tensor from (exactly representable, for pins) numeric values."""
     return torch.as_tensor(np.asarray(values, dtype=np.float32)).to(dtype)
+
+
+def block_mask_blocks(B: int, Hm: int, Sq: int, Sk: int, density: float, seed: int,
+                      keep_diagonal: bool = True, block: int = 128) -> np.ndarray:
+    """Seeded random block mask: bool ``[B, Hm, ceil(Sq/block), ceil(Sk/block)]``, each block marked with
+    probability ``density`` (blocks on the bottom-right-aligned diagonal always marked when ``keep_diagonal``)."""
+    rng = np.random.default_rng(int(seed))
+    QB, KB = -(-Sq // block), -(-Sk // block)
+    blocks = rng.random((B, Hm, QB, KB)) < density
+    if keep_diagonal:
+        off = (Sk - Sq) // block
+        for qb in range(QB):
+            kb = qb + off
+            if 0 <= kb < KB:
+                blocks[:, :, qb, kb] = True
+    return blocks

@@ -142,6 +142,61 @@ def attn_fwd_splitkv_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     return o, lse
 
 
+MASK_BLOCK = 128  # query rows and keys per block of a block mask (ATTN_MASK_BLOCK)
+
+
+def block_mask_words(B: int, mask_heads: int, Sq: int, Sk: int) -> int:
+    return int(load().attn_fwd_block_mask_words(B, mask_heads, Sq, Sk))
+
+
+def pack_block_mask(blocks: torch.Tensor) -> torch.Tensor:
+    """Bit-pack a boolean block mask ``[B, H, ceil(Sq/128), ceil(Sk/128)]`` into int32 words
+    ``[B, H, ceil(Sq/128), ceil(ceil(Sk/128)/32)]`` (bit ``kb % 32`` of word ``kb // 32``), on its device."""
+    if blocks.dim() != 4 or blocks.dtype != torch.bool:
+        raise ValueError("blocks must be a 4-d bool tensor [B, H, query blocks, key blocks]")
+    B, H, QB, KB = blocks.shape
+    W = (KB + 31) // 32
+    padded = torch.zeros((B, H, QB, W * 32), dtype=torch.int64, device=blocks.device)
+    padded[..., :KB] = blocks.to(torch.int64)
+    weights = torch.tensor([1 << b for b in range(32)], dtype=torch.int64, device=blocks.device)
+    words = (padded.view(B, H, QB, W, 32) * weights).sum(-1)
+    return (words - (words >= (1 << 31)).to(torch.int64) * (1 << 32)).to(torch.int32).contiguous()
+
+
+def attn_fwd_blocksparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: torch.Tensor,
+                         causal: int = 1, scale: float | None = None, o: torch.Tensor | None = None,
+                         lse: torch.Tensor | None = None, stream=None):
+    """Block-sparse forward: ``attn_fwd`` restricted to the marked (query block, key block) pairs.
+
+    ``block_mask``: contiguous int32 (or uint32) CUDA tensor ``[B, 1 or Hq, ceil(Sq/128), W]`` of
+    bit-packed words (see ``pack_block_mask``).  Returns ``(o, lse)``.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-d bf16 CUDA tensor")
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if block_mask.element_size() != 4 or not block_mask.is_cuda or not block_mask.is_contiguous() or \
+            block_mask.dim() != 4:
+        raise ValueError("block_mask must be a contiguous 4-d 32-bit CUDA tensor")
+    Hm = block_mask.shape[1]
+    W = (-(-Sk // MASK_BLOCK) + 31) // 32
+    if tuple(block_mask.shape) != (B, Hm, -(-Sq // MASK_BLOCK), W):
+        raise ValueError(f"block_mask shape {tuple(block_mask.shape)} does not fit q{tuple(q.shape)} k{tuple(k.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check(load().attn_fwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                       B, Hq, Hkv, Sq, Sk, D, int(causal), ctypes.c_float(scale),
+                                       block_mask.data_ptr(), int(Hm), _stream_handle(stream)))
+    return o, lse
+
+
 def debug_status(stream=None) -> tuple[int, int]:
     """Synchronise ``stream`` and read/clear the kernel's timeout word: ``(status, site)``."""
     site = ctypes.c_int(0)

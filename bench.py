@@ -36,7 +36,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from attention_forward_06_gb300.inputs import WORKLOADS, Workload, bf16_bits, draw_workload, sample_rows  # noqa: E402
+from attention_forward_06_gb300.inputs import (WORKLOADS, Workload, bf16_bits, block_mask_blocks,  # noqa: E402
+                                               draw_workload, sample_rows)
 
 METRIC = "attn fwd TFLOPS (bf16, 1×GB300) and % of dense-BF16 tensor peak; geomean"
 PERF_WORKLOADS = ["train", "gqa", "chunked128", "chunked64", "long"]
@@ -64,6 +65,24 @@ def conv_flops(w: Workload) -> float:
 
 def min_hbm_bytes(w: Workload) -> int:
     return 2 * w.B * (w.Hq * w.Sq * w.D * 2 + w.Hkv * w.Sk * w.D) + 4 * w.B * w.Hq * w.Sq
+
+
+def blocksparse_pairs(w: Workload, blocks: np.ndarray, block: int = 128) -> int:
+    """Unmasked (row, key) pairs under a block mask [B, Hm, QB, KB] and the workload's causal rule, summed over
+    every (batch, head)."""
+    i = np.arange(w.Sq)
+    last = np.full(w.Sq, w.Sk - 1) if w.causal == 0 else np.minimum(i + (w.Sk - w.Sq if w.causal == 1 else 0), w.Sk - 1)
+    total = 0
+    KB = blocks.shape[3]
+    for qb in range(blocks.shape[2]):
+        rows = last[qb * block:(qb + 1) * block]
+        # keys of key block kb visible to each row of the query block: clip(last + 1 - kb*block, 0, block)
+        per_kb = np.clip(rows[None, :] + 1 - (np.arange(KB) * block)[:, None], 0, block)
+        per_kb = np.minimum(per_kb, (w.Sk - np.arange(KB) * block)[:, None])
+        counts = per_kb.sum(axis=1)  # [KB]
+        marked = blocks[:, :, qb, :].astype(np.int64)  # [B, Hm, KB]
+        total += int((marked * counts).sum()) * (w.Hq // blocks.shape[1])
+    return total
 
 
 def row_flops(w: Workload, rows: np.ndarray) -> float:
@@ -356,9 +375,36 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         line["per_workload_tflops"] = per
         line["geomean_tflops"] = math.exp(sum(math.log(x) for x in per.values()) / len(per))
         line["geomean_pct_of_peak"] = 100.0 * line["geomean_tflops"] / peak
+        line["blocksparse"] = bench_blocksparse(stream, flush, dev, min(args.steps, 10))
     if world == 1 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     return line
+
+
+def bench_blocksparse(stream, flush, dev, steps: int, density: float = 0.25) -> dict:
+    """Block-sparse forward on the gqa shape with a quarter of the 128 x 128 blocks marked (the diagonal always),
+    against the dense kernel on the same inputs."""
+    from attention_forward_06_gb300 import ops
+
+    w = WORKLOADS["gqa"]
+    blocks = block_mask_blocks(w.B, w.Hq, w.Sq, w.Sk, density, seed=w.seed + 4000)
+    qx, kx, vx = [t.to(dev) for t in draw_workload(w)]
+    ox = torch.empty_like(qx)
+    lx = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    words = ops.pack_block_mask(torch.from_numpy(blocks).to(dev))
+
+    def fs():
+        ops.attn_fwd_blocksparse(qx, kx, vx, words, causal=w.causal, scale=w.scale, o=ox, lse=lx, stream=stream)
+
+    def fd():
+        ops.attn_fwd(qx, kx, vx, causal=w.causal, scale=w.scale, o=ox, lse=lx, stream=stream)
+
+    ts = statistics.mean(time_kernel(fs, steps, 3, flush, stream))
+    td = statistics.mean(time_kernel(fd, steps, 3, flush, stream))
+    flops = 4.0 * w.D * blocksparse_pairs(w, blocks)
+    return {"workload": f"{w.label()}, {density:.0%} of 128x128 blocks marked (diagonal always), per-head masks",
+            "tflops": flops / (ts * 1e-3) / 1e12, "ms": ts, "dense_ms": td, "speedup_vs_dense": td / ts,
+            "marked_fraction": float(blocks.mean())}
 
 
 def main():

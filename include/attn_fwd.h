@@ -46,6 +46,7 @@
 
 #include <cuda_runtime.h>
 #include <stddef.h>
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -127,6 +128,35 @@ int attn_fwd_splitkv_suggest(int B, int Hq, int Sq, int Sk, int D, int causal);
 int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                              int Hkv, int Sq, int Sk, int D, int causal, float scale, int n_splits,
                              cudaStream_t stream);
+
+/*
+ * Block-sparse forward: attn_fwd restricted to the (query block, key block)
+ * pairs a bit-packed mask marks.  Key j is visible to row i iff the causal rule
+ * allows it AND the mask bit of (query block i / ATTN_MASK_BLOCK, key block
+ * j / ATTN_MASK_BLOCK) is set; key blocks whose bit is clear are never loaded.
+ * This is the bit-packed block masking of page "AdaSplash-2: Faster
+ * Differentiable Sparse Attention" (technical summary section 2: one bit per
+ * block of the attention matrix, 32 blocks per 32-bit word, the output pass
+ * visiting only the marked blocks) applied to exact softmax attention.  A row
+ * with no visible key gets O = 0 and LSE = -inf.
+ *
+ * block_mask: device memory, 4-byte aligned, uint32 words laid out
+ *     [B][mask_heads][ceil(Sq / ATTN_MASK_BLOCK)][W],  W = ceil(ceil(Sk / ATTN_MASK_BLOCK) / 32),
+ * bit (kb % 32) of word (kb / 32) marking key block kb; bits past the last key
+ * block are ignored.  mask_heads is 1 (one mask for every head) or Hq.  The mask
+ * is read by the kernel and must not change until it has finished; it must not
+ * overlap o or lse.  Other arguments, layouts and status codes as attn_fwd
+ * (ATTN_ERR_INVALID_ARG also for a mask_heads that is neither 1 nor Hq).  One
+ * kernel is enqueued on `stream`; nothing is allocated.
+ */
+#define ATTN_MASK_BLOCK 128
+int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                         int Sq, int Sk, int D, int causal, float scale, const uint32_t* block_mask, int mask_heads,
+                         cudaStream_t stream);
+
+/* Number of uint32 words of a block mask for these sizes (layout above); 0 for
+   invalid sizes.  Host only, no CUDA call. */
+size_t attn_fwd_block_mask_words(int B, int mask_heads, int Sq, int Sk);
 
 /* Text for a status code.  For ATTN_ERR_CUDA it names the CUDA error of the
    calling thread's most recent failing call. */

@@ -144,3 +144,23 @@ def test_splitkv_invalid_arguments_before_any_device_work():
         ops.ATTN_ERR_INVALID_ARG
     assert lib.attn_fwd_splitkv(0, K, V, O, L, 1, 4, 2, 64, 64, 128, 1, 0.1, 2, W, 1 << 30, None) == \
         ops.ATTN_ERR_NULL_PTR
+
+
+def test_block_mask_words_formula():
+    lib = _lib.load()
+    for B, Hm, Sq, Sk in ((1, 1, 128, 128), (2, 4, 300, 5000), (1, 8, 1, 1), (3, 2, 257, 4097)):
+        qb, kb = -(-Sq // 128), -(-Sk // 128)
+        assert lib.attn_fwd_block_mask_words(B, Hm, Sq, Sk) == B * Hm * qb * ((kb + 31) // 32)
+    assert lib.attn_fwd_block_mask_words(1, 0, 128, 128) == 0
+    assert lib.attn_fwd_block_mask_words(-1, 1, 128, 128) == 0
+
+
+def test_blocksparse_invalid_arguments_before_any_device_work():
+    lib = _lib.load()
+    M = 0x700000  # fake, aligned mask address
+    args = lambda mask, heads: lib.attn_fwd_blocksparse(Q, K, V, O, L, 1, 4, 2, 64, 64, 128, 1, 0.1, mask, heads, None)
+    assert args(M, 3) == ops.ATTN_ERR_INVALID_ARG       # neither 1 nor Hq
+    assert args(M, 0) == ops.ATTN_ERR_INVALID_ARG
+    assert args(0, 1) == ops.ATTN_ERR_NULL_PTR
+    assert args(M + 2, 4) == ops.ATTN_ERR_MISALIGNED
+    assert args(O, 1) == ops.ATTN_ERR_INVALID_ARG       # the mask overlaps the output
