@@ -104,12 +104,14 @@ def from_values(values, dtype=torch.bfloat16) -> torch.Tensor:
 
 
 def block_mask_blocks(B: int, Hm: int, Sq: int, Sk: int, density: float, seed: int,
-                      keep_diagonal: bool = True, block: int = 128) -> np.ndarray:
+                      keep_diagonal: bool = True, block: int = 128, row_group: int = 1) -> np.ndarray:
     """Seeded random block mask: bool ``[B, Hm, ceil(Sq/block), ceil(Sk/block)]``, each block marked with
-    probability ``density`` (blocks on the bottom-right-aligned diagonal always marked when ``keep_diagonal``)."""
+    probability ``density`` (blocks on the bottom-right-aligned diagonal always marked when ``keep_diagonal``).
+    With ``row_group = g`` each run of g consecutive query blocks shares one draw (the same key blocks)."""
     rng = np.random.default_rng(int(seed))
     QB, KB = -(-Sq // block), -(-Sk // block)
-    blocks = rng.random((B, Hm, QB, KB)) < density
+    groups = rng.random((B, Hm, -(-QB // row_group), KB)) < density
+    blocks = np.repeat(groups, row_group, axis=2)[:, :, :QB]
     if keep_diagonal:
         off = (Sk - Sq) // block
         for qb in range(QB):

@@ -383,28 +383,33 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
 
 def bench_blocksparse(stream, flush, dev, steps: int, density: float = 0.25) -> dict:
     """Block-sparse forward on the gqa shape with a quarter of the 128 x 128 blocks marked (the diagonal always),
-    against the dense kernel on the same inputs."""
+    per-head masks, against the dense kernel on the same inputs: once with every query block drawn on its own, once
+    with pairs of query blocks (one 256-row work item) sharing their key blocks."""
     from attention_forward_06_gb300 import ops
 
     w = WORKLOADS["gqa"]
-    blocks = block_mask_blocks(w.B, w.Hq, w.Sq, w.Sk, density, seed=w.seed + 4000)
     qx, kx, vx = [t.to(dev) for t in draw_workload(w)]
     ox = torch.empty_like(qx)
     lx = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
-    words = ops.pack_block_mask(torch.from_numpy(blocks).to(dev))
-
-    def fs():
-        ops.attn_fwd_blocksparse(qx, kx, vx, words, causal=w.causal, scale=w.scale, o=ox, lse=lx, stream=stream)
 
     def fd():
         ops.attn_fwd(qx, kx, vx, causal=w.causal, scale=w.scale, o=ox, lse=lx, stream=stream)
 
-    ts = statistics.mean(time_kernel(fs, steps, 3, flush, stream))
     td = statistics.mean(time_kernel(fd, steps, 3, flush, stream))
-    flops = 4.0 * w.D * blocksparse_pairs(w, blocks)
-    return {"workload": f"{w.label()}, {density:.0%} of 128x128 blocks marked (diagonal always), per-head masks",
-            "tflops": flops / (ts * 1e-3) / 1e12, "ms": ts, "dense_ms": td, "speedup_vs_dense": td / ts,
-            "marked_fraction": float(blocks.mean())}
+    out = {"workload": f"{w.label()}, {density:.0%} of 128x128 blocks marked (diagonal always), per-head masks",
+           "dense_ms": td}
+    for name, group in (("independent_rows", 1), ("paired_rows", 2)):
+        blocks = block_mask_blocks(w.B, w.Hq, w.Sq, w.Sk, density, seed=w.seed + 4000, row_group=group)
+        words = ops.pack_block_mask(torch.from_numpy(blocks).to(dev))
+
+        def fs():
+            ops.attn_fwd_blocksparse(qx, kx, vx, words, causal=w.causal, scale=w.scale, o=ox, lse=lx, stream=stream)
+
+        ts = statistics.mean(time_kernel(fs, steps, 3, flush, stream))
+        flops = 4.0 * w.D * blocksparse_pairs(w, blocks)
+        out[name] = {"tflops": flops / (ts * 1e-3) / 1e12, "ms": ts, "speedup_vs_dense": td / ts,
+                     "marked_fraction": float(blocks.mean())}
+    return out
 
 
 def main():
