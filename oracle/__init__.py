@@ -3,6 +3,6 @@
 Only the tests, the smoke check and the benchmark's CPU-baseline leg import this
 package.  The product path (the CUDA library and its binding) never does.
 """
-from .attn_ref import attention, build, num_threads, probabilities
+from .attn_ref import attention, backward, build, num_threads, probabilities
 
-__all__ = ["attention", "build", "num_threads", "probabilities"]
+__all__ = ["attention", "backward", "build", "num_threads", "probabilities"]

@@ -228,3 +228,81 @@ int attn_ref_num_threads(void) {
     return 1;
 #endif
 }
+
+/*
+ * Backward of the forward above with respect to its output O (the gradient a
+ * training step carries; no gradient flows in through the LSE).  With the
+ * forward's probabilities P_ij (softmax over the allowed keys of row i) and the
+ * upstream gradient dO_i, by the chain rule through O_i = sum_j P_ij v_j and the
+ * softmax Jacobian dP_ij/ds_ik = P_ij (delta_jk - P_ik):
+ *     dV_j  = sum_i P_ij dO_i
+ *     dP_ij = dO_i . v_j
+ *     D_i   = sum_j P_ij dP_ij
+ *     dS_ij = P_ij (dP_ij - D_i)
+ *     dQ_i  = scale * sum_j dS_ij k_j
+ *     dK_j  = scale * sum_i dS_ij q_i
+ * where the sums over i run over every query head that reads the kv head.
+ * Inputs are bf16 bit patterns (dout like q); dq is [B][Hq][Sq][D], dk and dv
+ * [B][Hkv][Sk][D], all fp64.  Parallel over (batch, kv head), each of which owns
+ * its dk and dv rows.  Returns 0, 1 on bad arguments, 2 on allocation failure.
+ */
+int attn_ref_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                 double* dq, double* dk, double* dv,
+                 int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale) {
+    const int64_t G = (Hkv > 0) ? (int64_t)Hq / Hkv : 1;
+    const double scale64 = (double)scale;
+    int failed = 0;
+    int64_t bk;
+
+    if (check_args(B, Hq, Hkv, Sq, Sk, D, causal)) return 1;
+    memset(dq, 0, sizeof(double) * (size_t)B * Hq * Sq * D);
+    memset(dk, 0, sizeof(double) * (size_t)B * Hkv * Sk * D);
+    memset(dv, 0, sizeof(double) * (size_t)B * Hkv * Sk * D);
+
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (bk = 0; bk < (int64_t)B * Hkv; ++bk) {
+        const int64_t b = bk / Hkv, kvh = bk % Hkv;
+        const uint16_t* kh = k + bk * (int64_t)Sk * D;
+        const uint16_t* vh = v + bk * (int64_t)Sk * D;
+        double* dkh = dk + bk * (int64_t)Sk * D;
+        double* dvh = dv + bk * (int64_t)Sk * D;
+        double* s = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+        double* p = (double*)malloc(sizeof(double) * (size_t)(Sk > 0 ? Sk : 1));
+        double* orow = (double*)malloc(sizeof(double) * (size_t)(D > 0 ? D : 1));
+        int64_t g, i, j, d;
+        if (!s || !p || !orow) {
+            failed |= 1;
+            free(s); free(p); free(orow);
+            continue;
+        }
+        for (g = 0; g < G; ++g) {
+            const int64_t h = kvh * G + g;
+            for (i = 0; i < Sq; ++i) {
+                const int64_t r = (b * Hq + h) * (int64_t)Sq + i;
+                const uint16_t* qrow = q + r * D;
+                const uint16_t* dorow = dout + r * D;
+                const int64_t n = allowed_keys(i, Sq, Sk, causal);
+                double lse, Di = 0.0;
+                /* the forward's probabilities of this row (p is zero past the allowed keys) */
+                ref_row(qrow, kh, vh, i, Sq, Sk, D, causal, scale64, NULL, 1, s, p, orow, &lse);
+                if (n == 0) continue;
+                for (j = 0; j < n; ++j) {
+                    double dp = 0.0;
+                    for (d = 0; d < D; ++d) dp += bf16_bits_to_f64(dorow[d]) * bf16_bits_to_f64(vh[j * D + d]);
+                    s[j] = dp;  /* reuse: dP_ij */
+                    Di += p[j] * dp;
+                }
+                for (j = 0; j < n; ++j) {
+                    const double ds = p[j] * (s[j] - Di);
+                    for (d = 0; d < D; ++d) {
+                        dq[r * D + d] += scale64 * ds * bf16_bits_to_f64(kh[j * D + d]);
+                        dkh[j * D + d] += scale64 * ds * bf16_bits_to_f64(qrow[d]);
+                        dvh[j * D + d] += p[j] * bf16_bits_to_f64(dorow[d]);
+                    }
+                }
+            }
+        }
+        free(s); free(p); free(orow);
+    }
+    return failed ? 2 : 0;
+}

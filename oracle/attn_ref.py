@@ -59,6 +59,9 @@ def _load():
             lib.attn_ref_fwd_masked.restype = ctypes.c_int
             lib.attn_ref_fwd_masked.argtypes = [u16p, u16p, u16p, f64p, f64p] + [ctypes.c_int] * 7 + [
                 ctypes.c_float, ctypes.POINTER(ctypes.c_uint32)] + [ctypes.c_int] * 3 + [i64p, ctypes.c_int64]
+            lib.attn_ref_bwd.restype = ctypes.c_int
+            lib.attn_ref_bwd.argtypes = [u16p, u16p, u16p, u16p, f64p, f64p, f64p] + [ctypes.c_int] * 7 + [
+                ctypes.c_float]
             lib.attn_ref_probs.restype = ctypes.c_int
             lib.attn_ref_probs.argtypes = [u16p, u16p, u16p, f64p, f64p, f64p] + [ctypes.c_int] * 4 + [
                 ctypes.c_float]
@@ -148,3 +151,25 @@ def probabilities(q, k, v, causal: int, scale: float):
     if rc != 0:
         raise ValueError(f"attn_ref_probs failed with status {rc}")
     return p, o, lse
+
+
+def backward(q, k, v, dout, causal: int, scale: float):
+    """Gradients of the forward's O with respect to q, k, v for the upstream gradient ``dout`` (fp64).
+
+    ``q, dout [B,Hq,Sq,D]``, ``k, v [B,Hkv,Sk,D]`` as bf16 bit patterns.  Returns ``(dq, dk, dv)``.
+    """
+    q, k, v, dout = _u16(q), _u16(k), _u16(v), _u16(dout)
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    if k.shape != v.shape or Bk != B or Dk != D or dout.shape != q.shape:
+        raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape} dout{dout.shape}")
+    dq = np.empty((B, Hq, Sq, D), np.float64)
+    dk = np.empty((B, Hkv, Sk, D), np.float64)
+    dv = np.empty((B, Hkv, Sk, D), np.float64)
+    rc = _load().attn_ref_bwd(
+        _ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16), _ptr(dout, ctypes.c_uint16),
+        _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double),
+        B, Hq, Hkv, Sq, Sk, D, int(causal), float(np.float32(scale)))
+    if rc != 0:
+        raise ValueError(f"attn_ref_bwd failed with status {rc}")
+    return dq, dk, dv
