@@ -16,7 +16,7 @@ _libs: dict[str, ctypes.CDLL] = {}
 
 _c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
 
-# name -> (restype, argtypes), mirroring include/attn_fwd.h and include/attn_fwd_probe.h
+# name -> (restype, argtypes), mirroring include/attn_fwd.h, include/attn_bwd.h and include/attn_fwd_probe.h
 SIGNATURES = {
     "attn_fwd": {
         "attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
@@ -30,6 +30,12 @@ SIGNATURES = {
         "attn_fwd_splitkv_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _vp]),
         "attn_fwd_blocksparse": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp, _c_int, _vp]),
         "attn_fwd_block_mask_words": (ctypes.c_size_t, [_c_int] * 4),
+    },
+    "attn_bwd": {
+        "attn_bwd": (_c_int, [_vp] * 9 + [_c_int] * 7 + [_c_float, _vp, ctypes.c_size_t, _vp]),
+        "attn_bwd_workspace_size": (ctypes.c_size_t, [_c_int] * 3),
+        "attn_bwd_strerror": (ctypes.c_char_p, [_c_int]),
+        "attn_bwd_debug_status": (_c_int, [_vp, ctypes.POINTER(_c_int)]),
     },
     "attn_probe": {
         "attn_probe_mma_ss": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _vp, _vp]),

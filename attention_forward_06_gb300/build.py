@@ -1,9 +1,10 @@
 """Build the CUDA libraries in-tree with nvcc (sm_103a only).
 
     libattn_fwd.so    the attention forward pass (C ABI: include/attn_fwd.h)
-    libattn_probe.so  primitive checks of its building blocks (include/attn_fwd_probe.h)
+    libattn_bwd.so    its backward (C ABI: include/attn_bwd.h)
+    libattn_probe.so  primitive checks of their building blocks (include/attn_fwd_probe.h)
 
-Both translation units compile in parallel; a library is rebuilt only when a
+The translation units compile in parallel; a library is rebuilt only when a
 source or header is newer than it.  Usage: ``python -m attention_forward_06_gb300.build``.
 """
 from __future__ import annotations
@@ -29,6 +30,7 @@ NVCC_FLAGS = ARCH + [
 
 LIBS = {
     "attn_fwd": os.path.join(CSRC, "attn_fwd.cu"),
+    "attn_bwd": os.path.join(CSRC, "attn_bwd.cu"),
     "attn_probe": os.path.join(CSRC, "probe.cu"),
 }
 

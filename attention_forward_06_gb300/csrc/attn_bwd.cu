@@ -1,0 +1,802 @@
+// attn_bwd.cu -- backward of the exact attention forward pass for GB300 (sm_103a):
+// the gradients of O = softmax(scale * Q K^T + mask) V with respect to Q, K and V
+// for an upstream gradient dO, from the forward's saved LSE (the softmax with a
+// closed-form log-sum-exp normaliser of page "AdaSplash-2: Faster Differentiable
+// Sparse Attention", technical summary section 1; its summary notes that the
+// backward pass, too, visits only the blocks it needs).  With P_ij recomputed as
+// exp(scale q_i.k_j - LSE_i):
+//     dV_j = sum_i P_ij dO_i,   dP_ij = dO_i . v_j,   D_i = dO_i . O_i,
+//     dS_ij = P_ij (dP_ij - D_i),   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i.
+//
+// Three kernels on the caller's stream:
+//   attn_bwd_prep_kernel   D_i = dO_i . O_i and LSE_i * log2(e) into the workspace
+//                          (+inf for rows without keys and for padding rows, so their P is 0)
+//   attn_bwd_dkdv_kernel   one (batch, kv head, 128-key tile) per work item: streams the
+//                          query tiles of every query head of the group, with the keys in
+//                          the TMEM lanes: S^T = K Q^T and dP^T = V dO^T (SS form), P^T and
+//                          dS^T written back as bf16, then dV += P^T dO and dK += dS^T Q (TS
+//                          form, A from TMEM) accumulate in TMEM across the whole item
+//   attn_bwd_dq_kernel     one (batch, query head, 128-row tile) per item: S = Q K^T,
+//                          dP = dO V^T, dS into TMEM, dQ += dS K
+// Each kernel: warps 0-3 compute (one thread per TMEM lane), warp 4 loads with TMA,
+// warp 5 issues the tcgen05 MMAs; every wait is bounded as in the forward.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_bwd.h"
+#include "host_util.h"
+#include "ptx.cuh"
+
+using namespace attn;
+
+namespace {
+
+constexpr int BT = 128;  // query rows / keys per tile (MMA M and N)
+constexpr int kThreads = 192;
+constexpr int kLoadWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kRing = 2;  // streamed tile-pair slots
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kTimeoutNs = 4000000000ull;
+constexpr uint64_t kDrainTimeoutNs = 500000000ull;
+constexpr int kSiteProducer = 1, kSiteIssuer = 2, kSiteCompute = 3;
+
+template <int D>
+struct BCfg {
+  static constexpr int kTileBytes = BT * D * 2;    // one 128-row bf16 tile
+  static constexpr int kColBlockBytes = BT * 128;  // 64 columns x 128 rows, 128-B swizzled
+  static constexpr int kVecBytes = BT * 4;         // 128 fp32 values
+  static constexpr int kSlotBytes = 2 * kTileBytes + 2 * kVecBytes;
+  static constexpr int kSmemBytes = 2 * kTileBytes + kRing * kSlotBytes + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+struct BParams {
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const float* lse2;   // [B*Hq][Sq_pad]: LSE * log2(e), +inf where P must be 0
+  const float* delta;  // [B*Hq][Sq_pad]: dO . O
+  int Hq, Hkv, G, Sq, Sk, Sq_pad;
+  int causal, diag;  // key j visible to row i iff !causal or j <= i + diag
+  int n_qt, n_kt;    // 128-row query tiles, 128-key tiles
+  int BZ;            // B * Hkv (dK/dV items) ...
+  int BH;            // ... and B * Hq (dQ items)
+  int n_items;
+  float c;      // scale * log2(e)
+  float scale;
+};
+
+__device__ int g_bwd_status;
+
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                          uint64_t timeout_ns) {
+  const bool ok = mbar_wait_bounded(bar, parity, abort_flag, timeout_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void record_abort(volatile uint32_t* abort_flag, int site) {
+  *abort_flag = 1;
+  atomicCAS(&g_bwd_status, 0, site);
+}
+
+// ---------------------------------------------------------------------------- prep
+// One warp per (row of B*Hq*Sq_pad): D_i = sum_d dO[i,d] O[i,d] (fp32, from the bf16 tensors)
+// and LSE_i * log2(e); rows past Sq and rows without keys (LSE = -inf) get +inf.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                            const __nv_bfloat16* __restrict__ dout,
+                                                            const float* __restrict__ lse, float* __restrict__ lse2,
+                                                            float* __restrict__ delta, int64_t BH, int Sq,
+                                                            int Sq_pad) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= BH * Sq_pad) return;
+  const int64_t bh = row / Sq_pad;
+  const int i = static_cast<int>(row % Sq_pad);
+  float acc = 0.0f, l2 = INFINITY;
+  if (i < Sq) {
+    const int64_t r = bh * Sq + i;
+    const uint32_t* o2 = reinterpret_cast<const uint32_t*>(o + r * D);
+    const uint32_t* g2 = reinterpret_cast<const uint32_t*>(dout + r * D);
+#pragma unroll
+    for (int e = lane; e < D / 2; e += 32) {
+      const uint32_t a = o2[e], b = g2[e];
+      acc = fmaf(bf16lo_to_f32(a), bf16lo_to_f32(b), acc);
+      acc = fmaf(bf16hi_to_f32(a), bf16hi_to_f32(b), acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const float L = lse[r];
+    l2 = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+  }
+  if (lane == 0) {
+    lse2[row] = l2;
+    delta[row] = acc;
+  }
+}
+
+// Query tiles [i0, n_qt) that see key tile j (none when i0 >= n_qt).
+__device__ __forceinline__ int first_qtile(const BParams& p, int j) {
+  if (!p.causal) return 0;
+  const int first_row = BT * j - p.diag;  // row i sees key 128 j iff i + diag >= 128 j
+  if (first_row <= 0) return 0;
+  if (first_row >= p.Sq) return p.n_qt;
+  return first_row / BT;
+}
+
+// ---------------------------------------------------------------------------- dK, dV
+// Work item x: key tile j = x / (B*Hkv) (ascending: under a causal mask the
+// heaviest first), kv slice z = x % (B*Hkv).  TMEM (lane = key): S^T [0,128),
+// dP^T [128,256), dV [256,256+D), dK [384,384+D); P^T and dS^T (bf16 pairs)
+// overwrite the first 64 columns of S^T and dP^T.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                         const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                         const BParams p) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  uint8_t* k_s = smem;
+  uint8_t* v_s = smem + C::kTileBytes;
+  uint8_t* ring = smem + 2 * C::kTileBytes;  // slot: Q, dO, lse2[128], delta[128]
+  __shared__ uint64_t kv_full, kv_empty, full[kRing], empty[kRing], st_full, pt_full, acc_full, acc_empty, drain;
+  __shared__ uint32_t tmem_slot, abort_flag;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nz = p.BZ;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&kv_full, 1);
+    mbar_init(&kv_empty, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&st_full, 1);
+    mbar_init(&pt_full, 4 * 32);
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, 4 * 32);
+    mbar_init(&drain, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile uint32_t* abort_v = &abort_flag;
+  const int G = p.G;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ TMA producer
+    uint32_t it = 0, n_ne = 0;  // ring loads issued; items with query tiles
+    bool ok = true;
+    for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
+      const int j = x / nz, z = x % nz;
+      const int i0 = first_qtile(p, j);
+      const int nI = p.n_qt - i0;
+      if (nI <= 0) continue;
+      if (n_ne > 0) ok = warp_wait(&kv_empty, (n_ne - 1) & 1, abort_v, kTimeoutNs);
+      if (!ok) break;
+      mbar_arrive_expect_tx_elect(&kv_full, 2 * C::kTileBytes);
+#pragma unroll
+      for (int cb = 0; cb < D / 64; ++cb) {
+        tma_load_3d_elect(k_s + cb * C::kColBlockBytes, &tk, &kv_full, cb * 64, j * BT, z);
+        tma_load_3d_elect(v_s + cb * C::kColBlockBytes, &tv, &kv_full, cb * 64, j * BT, z);
+      }
+      ++n_ne;
+      const int b = z / p.Hkv, kvh = z % p.Hkv;
+      for (int s = 0; s < G * nI && ok; ++s, ++it) {
+        const int h = kvh * G + s / nI, i = i0 + s % nI;
+        const int bh = b * p.Hq + h;
+        const uint32_t slot = it % kRing, use = it / kRing;
+        if (use > 0) ok = warp_wait(&empty[slot], (use - 1) & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        uint8_t* sl = ring + slot * C::kSlotBytes;
+        mbar_arrive_expect_tx_elect(&full[slot], 2 * C::kTileBytes + 2 * C::kVecBytes);
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb) {
+          tma_load_3d_elect(sl + cb * C::kColBlockBytes, &tq, &full[slot], cb * 64, i * BT, bh);
+          tma_load_3d_elect(sl + C::kTileBytes + cb * C::kColBlockBytes, &tdo, &full[slot], cb * 64, i * BT, bh);
+        }
+        const int64_t voff = static_cast<int64_t>(bh) * p.Sq_pad + i * BT;
+        bulk_load_1d_elect(sl + 2 * C::kTileBytes, p.lse2 + voff, C::kVecBytes, &full[slot]);
+        bulk_load_1d_elect(sl + 2 * C::kTileBytes + C::kVecBytes, p.delta + voff, C::kVecBytes, &full[slot]);
+      }
+    }
+    if (!ok) {
+      if (lane == 0) record_abort(abort_v, kSiteProducer);
+      for (uint32_t u = (it > kRing ? it - kRing : 0); u < it; ++u)
+        mbar_wait_bounded(&full[u % kRing], (u / kRing) & 1, abort_v, kDrainTimeoutNs);
+      if (n_ne > 0) mbar_wait_bounded(&kv_full, (n_ne - 1) & 1, abort_v, kDrainTimeoutNs);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ tcgen05 issuer
+    const uint32_t idesc_s = idesc_bf16_f32(BT, BT, false);
+    const uint32_t idesc_acc = idesc_bf16_f32(BT, D, true);
+    const uint32_t k_addr = smem_u32(k_s), v_addr = smem_u32(v_s), ring_addr = smem_u32(ring);
+    uint32_t it = 0, gs = 0, n_ne = 0;  // ring uses, steps (st/pt phases), items with query tiles
+    bool ok = true;
+    for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
+      const int j = x / nz;
+      const int nI = p.n_qt - first_qtile(p, j);
+      if (nI <= 0) continue;
+      ok = warp_wait(&kv_full, n_ne & 1, abort_v, kTimeoutNs);
+      if (!ok) break;
+      const uint64_t kd = sdesc_sw128(k_addr, 16, 1024), vd = sdesc_sw128(v_addr, 16, 1024);
+      for (int s = 0; s < G * nI; ++s, ++it, ++gs) {
+        const uint32_t slot = it % kRing;
+        const uint32_t q_addr = opaque(ring_addr) + slot * C::kSlotBytes;
+        const uint32_t do_addr = q_addr + C::kTileBytes;
+        ok = warp_wait(&full[slot], (it / kRing) & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        // S^T = K Q^T and dP^T = V dO^T (keys in the TMEM lanes), K steps over D
+        const uint64_t qd = sdesc_sw128(q_addr, 16, 1024), dod = sdesc_sw128(do_addr, 16, 1024);
+        if constexpr (D == 128) {
+          mma_bf16_ss_k8(tmem, kd, qd, idesc_s);
+          mma_bf16_ss_k8(tmem + BT, vd, dod, idesc_s, smem_u32(&st_full));
+        } else {
+          mma_bf16_ss_k4(tmem, kd, qd, idesc_s);
+          mma_bf16_ss_k4(tmem + BT, vd, dod, idesc_s, smem_u32(&st_full));
+        }
+        ok = warp_wait(&pt_full, gs & 1, abort_v, kTimeoutNs);
+        if (ok && s == 0 && n_ne > 0) ok = warp_wait(&acc_empty, (n_ne - 1) & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        // dV += P^T dO and dK += dS^T Q: A from TMEM, B (dO, Q) MN-major over the query rows
+        const uint64_t dob = sdesc_sw128(do_addr, C::kColBlockBytes, 1024);
+        const uint64_t qb = sdesc_sw128(q_addr, C::kColBlockBytes, 1024);
+        mma_bf16_ts_k8(tmem + 2 * BT, tmem, dob, idesc_acc, s > 0 ? 1u : 0u);
+        mma_bf16_ts_k8(tmem + 3 * BT, tmem + BT, qb, idesc_acc, s > 0 ? 1u : 0u, smem_u32(&empty[slot]),
+                       s + 1 == G * nI ? smem_u32(&acc_full) : kNoBar);
+      }
+      if (!ok) break;
+      mma_commit_elect(&kv_empty);  // K and V of this item are no longer read
+      ++n_ne;
+    }
+    if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
+    mma_commit_elect(&drain);
+    warp_wait(&drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
+  } else {
+    // ------------------------------------------------------------ compute (one thread per key)
+    const int quarter = warp;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t st_t = tmem + lane_off, dpt_t = tmem + lane_off + BT;
+    const uint32_t dv_t = tmem + lane_off + 2 * BT, dk_t = tmem + lane_off + 3 * BT;
+    const int kk = quarter * 32 + lane;
+    uint32_t it = 0, gs = 0, n_ne = 0;
+    bool ok = true;
+    for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
+      const int j = x / nz, z = x % nz;
+      const int i0 = first_qtile(p, j);
+      const int nI = p.n_qt - i0;
+      const int key = j * BT + kk;
+      const bool key_live = key < p.Sk;
+      __nv_bfloat16* dvrow = p.dv + (static_cast<int64_t>(z) * p.Sk + key) * D;
+      __nv_bfloat16* dkrow = p.dk + (static_cast<int64_t>(z) * p.Sk + key) * D;
+      if (nI <= 0) {  // no query row sees this key tile: zero gradients
+        if (key_live) {
+          uint4* a = reinterpret_cast<uint4*>(dvrow);
+          uint4* b2 = reinterpret_cast<uint4*>(dkrow);
+#pragma unroll
+          for (int v4 = 0; v4 < D / 8; ++v4) a[v4] = b2[v4] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
+      for (int s = 0; s < G * nI; ++s, ++it, ++gs) {
+        const int i = i0 + s % nI;
+        const int row0 = i * BT;
+        const uint8_t* sl = ring + (it % kRing) * C::kSlotBytes;
+        const float* lse2v = reinterpret_cast<const float*>(sl + 2 * C::kTileBytes);
+        const float* deltav = lse2v + BT;
+        // the slot's vectors have landed (this warp observes their copy itself), then S^T and dP^T
+        ok = warp_wait(&full[it % kRing], (it / kRing) & 1, abort_v, kTimeoutNs);
+        if (ok) ok = warp_wait(&st_full, gs & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        // elements to mask: keys past Sk, and keys above the diagonal of a straddling tile
+        const bool diag_tile = p.causal && (j * BT + BT - 1 > row0 + p.diag);
+        const int first_ok_row = key - p.diag - row0;  // rows r >= this see the key (diagonal tiles)
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t sv[32], dpv[32], pk[16], dsk[16];
+          tmem_ld32_wait(st_t + 32 * c4, sv);
+          tmem_ld32_wait(dpt_t + 32 * c4, dpv);
+#pragma unroll
+          for (int r2 = 0; r2 < 16; ++r2) {
+            const int r = 32 * c4 + 2 * r2;
+            float pp[2], dd[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const bool vis = key_live && (!diag_tile || r + h >= first_ok_row);
+              const float pr = vis ? ex2_approx(fmaf(__uint_as_float(sv[2 * r2 + h]), p.c, -lse2v[r + h])) : 0.0f;
+              pp[h] = pr;
+              dd[h] = pr * (__uint_as_float(dpv[2 * r2 + h]) - deltav[r + h]);
+            }
+            pk[r2] = pack_bf16x2(pp[0], pp[1]);
+            dsk[r2] = pack_bf16x2(dd[0], dd[1]);
+          }
+          tmem_st16(st_t + 16 * c4, pk);
+          tmem_st16(dpt_t + 16 * c4, dsk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&pt_full);
+      }
+      if (!ok) break;
+      // epilogue: dV and scale * dK of this key, bf16, once the item's last MMAs are done
+      ok = warp_wait(&acc_full, n_ne & 1, abort_v, kTimeoutNs);
+      if (!ok) break;
+      ++n_ne;
+      tc_fence_after();
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const float mul = which == 0 ? 1.0f : p.scale;
+        __nv_bfloat16* dst = which == 0 ? dvrow : dkrow;
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t a[32];
+          tmem_ld32_wait((which == 0 ? dv_t : dk_t) + 32 * cb, a);
+          if (key_live) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cb);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t w[4];
+#pragma unroll
+              for (int h = 0; h < 4; ++h)
+                w[h] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * h]) * mul,
+                                   __uint_as_float(a[8 * q4 + 2 * h + 1]) * mul);
+              d4[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty);  // dV and dK may be overwritten by the next item
+    }
+    if (!ok && lane == 0) record_abort(abort_v, kSiteCompute);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Key tiles query tile i visits: [0, n).
+__device__ __forceinline__ int key_tiles(const BParams& p, int i) {
+  if (!p.causal) return p.n_kt;
+  const int last_row = min(i * BT + BT, p.Sq) - 1;
+  const int kv_end = min(p.Sk, last_row + p.diag + 1);
+  return kv_end > 0 ? (kv_end + BT - 1) / BT : 0;
+}
+
+// ---------------------------------------------------------------------------- dQ
+// Work item x: query tile i = n_qt - 1 - x / (B*Hq) (heaviest first under a causal
+// mask), slice bh = x % (B*Hq).  TMEM (lane = query row): S [0,128), dP [128,256),
+// dQ [256,256+D); dS (bf16 pairs) overwrites the first 64 columns of S.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                       const BParams p) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  uint8_t* q_s = smem;
+  uint8_t* do_s = smem + C::kTileBytes;
+  uint8_t* ring = smem + 2 * C::kTileBytes;  // slot: K, V
+  __shared__ uint64_t qd_full, qd_empty, full[kRing], empty[kRing], s_full, ds_full, acc_full, acc_empty, drain;
+  __shared__ uint32_t tmem_slot, abort_flag;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&qd_full, 1);
+    mbar_init(&qd_empty, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&s_full, 1);
+    mbar_init(&ds_full, 4 * 32);
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, 4 * 32);
+    mbar_init(&drain, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile uint32_t* abort_v = &abort_flag;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ TMA producer
+    uint32_t it = 0, n_ne = 0;
+    bool ok = true;
+    for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
+      const int i = p.n_qt - 1 - x / p.BH, bh = x % p.BH;
+      const int n = key_tiles(p, i);
+      if (n <= 0) continue;
+      if (n_ne > 0) ok = warp_wait(&qd_empty, (n_ne - 1) & 1, abort_v, kTimeoutNs);
+      if (!ok) break;
+      mbar_arrive_expect_tx_elect(&qd_full, 2 * C::kTileBytes);
+#pragma unroll
+      for (int cb = 0; cb < D / 64; ++cb) {
+        tma_load_3d_elect(q_s + cb * C::kColBlockBytes, &tq, &qd_full, cb * 64, i * BT, bh);
+        tma_load_3d_elect(do_s + cb * C::kColBlockBytes, &tdo, &qd_full, cb * 64, i * BT, bh);
+      }
+      ++n_ne;
+      const int kvz = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.G;
+      for (int j = 0; j < n && ok; ++j, ++it) {
+        const uint32_t slot = it % kRing, use = it / kRing;
+        if (use > 0) ok = warp_wait(&empty[slot], (use - 1) & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        uint8_t* sl = ring + slot * C::kSlotBytes;
+        mbar_arrive_expect_tx_elect(&full[slot], 2 * C::kTileBytes);
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb) {
+          tma_load_3d_elect(sl + cb * C::kColBlockBytes, &tk, &full[slot], cb * 64, j * BT, kvz);
+          tma_load_3d_elect(sl + C::kTileBytes + cb * C::kColBlockBytes, &tv, &full[slot], cb * 64, j * BT, kvz);
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) record_abort(abort_v, kSiteProducer);
+      for (uint32_t u = (it > kRing ? it - kRing : 0); u < it; ++u)
+        mbar_wait_bounded(&full[u % kRing], (u / kRing) & 1, abort_v, kDrainTimeoutNs);
+      if (n_ne > 0) mbar_wait_bounded(&qd_full, (n_ne - 1) & 1, abort_v, kDrainTimeoutNs);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ tcgen05 issuer
+    const uint32_t idesc_s = idesc_bf16_f32(BT, BT, false);
+    const uint32_t idesc_acc = idesc_bf16_f32(BT, D, true);
+    const uint64_t qd = sdesc_sw128(smem_u32(q_s), 16, 1024), dod = sdesc_sw128(smem_u32(do_s), 16, 1024);
+    const uint32_t ring_addr = smem_u32(ring);
+    uint32_t it = 0, gs = 0, n_ne = 0;
+    bool ok = true;
+    for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
+      const int n = key_tiles(p, p.n_qt - 1 - x / p.BH);
+      if (n <= 0) continue;
+      ok = warp_wait(&qd_full, n_ne & 1, abort_v, kTimeoutNs);
+      if (!ok) break;
+      for (int j = 0; j < n; ++j, ++it, ++gs) {
+        const uint32_t slot = it % kRing;
+        const uint32_t k_addr = opaque(ring_addr) + slot * C::kSlotBytes, v_addr = k_addr + C::kTileBytes;
+        ok = warp_wait(&full[slot], (it / kRing) & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        // S = Q K^T and dP = dO V^T (rows in the TMEM lanes), K steps over D
+        const uint64_t kd = sdesc_sw128(k_addr, 16, 1024), vd = sdesc_sw128(v_addr, 16, 1024);
+        if constexpr (D == 128) {
+          mma_bf16_ss_k8(tmem, qd, kd, idesc_s);
+          mma_bf16_ss_k8(tmem + BT, dod, vd, idesc_s, smem_u32(&s_full));
+        } else {
+          mma_bf16_ss_k4(tmem, qd, kd, idesc_s);
+          mma_bf16_ss_k4(tmem + BT, dod, vd, idesc_s, smem_u32(&s_full));
+        }
+        ok = warp_wait(&ds_full, gs & 1, abort_v, kTimeoutNs);
+        if (ok && j == 0 && n_ne > 0) ok = warp_wait(&acc_empty, (n_ne - 1) & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        // dQ += dS K: A (dS) from TMEM, B (K) MN-major over the keys
+        const uint64_t kb = sdesc_sw128(k_addr, C::kColBlockBytes, 1024);
+        mma_bf16_ts_k8(tmem + 2 * BT, tmem, kb, idesc_acc, j > 0 ? 1u : 0u, smem_u32(&empty[slot]),
+                       j + 1 == n ? smem_u32(&acc_full) : kNoBar);
+      }
+      if (!ok) break;
+      mma_commit_elect(&qd_empty);  // Q and dO of this item are no longer read
+      ++n_ne;
+    }
+    if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
+    mma_commit_elect(&drain);
+    warp_wait(&drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
+  } else {
+    // ------------------------------------------------------------ compute (one thread per query row)
+    const int quarter = warp;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t s_t = tmem + lane_off, dp_t = tmem + lane_off + BT, dq_t = tmem + lane_off + 2 * BT;
+    uint32_t gs = 0, n_ne = 0;
+    bool ok = true;
+    for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
+      const int i = p.n_qt - 1 - x / p.BH, bh = x % p.BH;
+      const int n = key_tiles(p, i);
+      const int row = i * BT + quarter * 32 + lane;
+      const bool live = row < p.Sq;
+      __nv_bfloat16* dqrow = p.dq + (static_cast<int64_t>(bh) * p.Sq + row) * D;
+      if (n <= 0) {  // no key is visible to any row of this tile: zero gradient
+        if (live) {
+          uint4* a = reinterpret_cast<uint4*>(dqrow);
+#pragma unroll
+          for (int v4 = 0; v4 < D / 8; ++v4) a[v4] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
+      const float lse2 = p.lse2[static_cast<int64_t>(bh) * p.Sq_pad + row];
+      const float delt = p.delta[static_cast<int64_t>(bh) * p.Sq_pad + row];
+      const int lim = p.causal ? min(p.Sk - 1, row + p.diag) : p.Sk - 1;  // last visible key
+      for (int j = 0; j < n; ++j, ++gs) {
+        ok = warp_wait(&s_full, gs & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        const int kmax = lim - j * BT;  // keys of this tile past kmax are masked
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t sv[32], dpv[32], dsk[16];
+          tmem_ld32_wait(s_t + 32 * c4, sv);
+          tmem_ld32_wait(dp_t + 32 * c4, dpv);
+#pragma unroll
+          for (int e2 = 0; e2 < 16; ++e2) {
+            float dd[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = 32 * c4 + 2 * e2 + h;
+              const float pr = e <= kmax ? ex2_approx(fmaf(__uint_as_float(sv[2 * e2 + h]), p.c, -lse2)) : 0.0f;
+              dd[h] = pr * (__uint_as_float(dpv[2 * e2 + h]) - delt);
+            }
+            dsk[e2] = pack_bf16x2(dd[0], dd[1]);
+          }
+          tmem_st16(s_t + 16 * c4, dsk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&ds_full);
+      }
+      if (!ok) break;
+      ok = warp_wait(&acc_full, n_ne & 1, abort_v, kTimeoutNs);
+      if (!ok) break;
+      ++n_ne;
+      tc_fence_after();
+#pragma unroll
+      for (int cb = 0; cb < D / 32; ++cb) {
+        uint32_t a[32];
+        tmem_ld32_wait(dq_t + 32 * cb, a);
+        if (live) {
+          uint4* d4 = reinterpret_cast<uint4*>(dqrow + 32 * cb);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+              w[h] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * h]) * p.scale,
+                                 __uint_as_float(a[8 * q4 + 2 * h + 1]) * p.scale);
+            d4[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty);
+    }
+    if (!ok && lane == 0) record_abort(abort_v, kSiteCompute);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = e;
+  return ATTN_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+int g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 unsupported
+int g_dev_sms[kMaxDevices];
+
+int prepare_device(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_dev_state[dev] == 1) return ATTN_OK;
+  if (g_dev_state[dev] == -1) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  int major = 0, minor = 0, sms = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (major != 10 || minor != 3) {
+    g_dev_state[dev] = -1;
+    return ATTN_ERR_UNSUPPORTED_DEVICE;
+  }
+  g_dev_sms[dev] = sms;
+  const void* fns[] = {reinterpret_cast<const void*>(attn_bwd_dkdv_kernel<128>),
+                       reinterpret_cast<const void*>(attn_bwd_dq_kernel<128>),
+                       reinterpret_cast<const void*>(attn_bwd_dkdv_kernel<64>),
+                       reinterpret_cast<const void*>(attn_bwd_dq_kernel<64>)};
+  const int bytes[] = {BCfg<128>::kSmemBytes, BCfg<128>::kSmemBytes, BCfg<64>::kSmemBytes, BCfg<64>::kSmemBytes};
+  for (int f = 0; f < 4 && e == cudaSuccess; ++f)
+    e = cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes[f]);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (!attn_host::encode_tiled_fn()) return ATTN_ERR_TENSOR_MAP;
+  g_dev_state[dev] = 1;
+  return ATTN_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool misaligned(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; }
+
+int64_t padded_rows(int Sq) { return (static_cast<int64_t>(Sq) + BT - 1) / BT * BT; }
+
+template <int D>
+int launch_all(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+               BParams prm, const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* lse, float* lse2,
+               float* delta, int sms, cudaStream_t stream) {
+  const int64_t prep_rows = static_cast<int64_t>(prm.BH) * prm.Sq_pad;
+  attn_bwd_prep_kernel<D><<<static_cast<unsigned>((prep_rows + 7) / 8), 256, 0, stream>>>(
+      o, dout, lse, lse2, delta, prm.BH, prm.Sq, prm.Sq_pad);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  BParams a = prm;
+  a.n_items = prm.n_kt * prm.BZ;
+  attn_bwd_dkdv_kernel<D><<<a.n_items < sms ? a.n_items : sms, kThreads, BCfg<D>::kSmemBytes, stream>>>(tq, tk, tv,
+                                                                                                     tdo, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  BParams b = prm;
+  b.n_items = prm.n_qt * prm.BH;
+  attn_bwd_dq_kernel<D><<<b.n_items < sms ? b.n_items : sms, kThreads, BCfg<D>::kSmemBytes, stream>>>(tq, tk, tv,
+                                                                                                   tdo, b);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Sq) {
+  if (B < 0 || Hq < 1 || Sq < 0) return 0;
+  const size_t one = static_cast<size_t>(B) * Hq * padded_rows(Sq) * 4;
+  return 2 * ((one + 255) & ~static_cast<size_t>(255));
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+             void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  // ---- argument checks (host only, before any CUDA call)
+  if (B < 0 || Sq < 0 || Sk < 0 || Hq < 1 || Hkv < 1) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || causal < 0 || causal > 2 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * Hq > INT32_MAX / 2 || padded_rows(Sq) > INT32_MAX / 2) return ATTN_ERR_INVALID_ARG;
+  if (B == 0) return ATTN_OK;
+  const size_t qb = static_cast<size_t>(B) * Hq * Sq * D * 2, kb = static_cast<size_t>(B) * Hkv * Sk * D * 2;
+  const size_t lb = static_cast<size_t>(B) * Hq * Sq * 4;
+  const size_t wb = attn_bwd_workspace_size(B, Hq, Sq);
+  if (Sq > 0 && (!q || !o || !lse || !dout || !dq)) return ATTN_ERR_NULL_PTR;
+  if (Sk > 0 && (!k || !v || !dk || !dv)) return ATTN_ERR_NULL_PTR;
+  if (Sq > 0 && Sk > 0 && !workspace) return ATTN_ERR_NULL_PTR;
+  const void* al[] = {q, k, v, o, lse, dout, dq, dk, dv, workspace};
+  for (const void* ptr : al)
+    if (ptr && misaligned(ptr)) return ATTN_ERR_MISALIGNED;
+  if (Sq > 0 && Sk > 0 && workspace_bytes < wb) return ATTN_ERR_INVALID_ARG;
+  // outputs (and the workspace) must not overlap each other or any input
+  const void* outs[] = {dq, dk, dv, workspace};
+  const size_t out_n[] = {qb, kb, kb, wb};
+  const void* ins[] = {q, k, v, o, lse, dout};
+  const size_t in_n[] = {qb, kb, kb, qb, lb, qb};
+  for (int a = 0; a < 4; ++a) {
+    for (int b2 = 0; b2 < 6; ++b2)
+      if (overlaps(outs[a], out_n[a], ins[b2], in_n[b2])) return ATTN_ERR_INVALID_ARG;
+    for (int b2 = a + 1; b2 < 4; ++b2)
+      if (overlaps(outs[a], out_n[a], outs[b2], out_n[b2])) return ATTN_ERR_INVALID_ARG;
+  }
+
+  // ---- device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int st = prepare_device(dev);
+  if (st != ATTN_OK) return st;
+  if (Sq == 0 || Sk == 0) {  // no (row, key) pair: the gradients that exist are zero
+    if (Sk > 0) {
+      if ((e = cudaMemsetAsync(dk, 0, kb, stream)) != cudaSuccess) return cuda_fail(e);
+      if ((e = cudaMemsetAsync(dv, 0, kb, stream)) != cudaSuccess) return cuda_fail(e);
+    }
+    if (Sq > 0 && (e = cudaMemsetAsync(dq, 0, qb, stream)) != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+  }
+
+  CUtensorMap tq, tk, tv, tdo;
+  if (!attn_host::encode_bf16_rows(&tq, q, D, Sq, static_cast<uint64_t>(B) * Hq, BT) ||
+      !attn_host::encode_bf16_rows(&tdo, dout, D, Sq, static_cast<uint64_t>(B) * Hq, BT) ||
+      !attn_host::encode_bf16_rows(&tk, k, D, Sk, static_cast<uint64_t>(B) * Hkv, BT) ||
+      !attn_host::encode_bf16_rows(&tv, v, D, Sk, static_cast<uint64_t>(B) * Hkv, BT))
+    return ATTN_ERR_TENSOR_MAP;
+
+  BParams prm;
+  prm.dq = static_cast<__nv_bfloat16*>(dq);
+  prm.dk = static_cast<__nv_bfloat16*>(dk);
+  prm.dv = static_cast<__nv_bfloat16*>(dv);
+  const size_t one = wb / 2;
+  float* lse2 = static_cast<float*>(workspace);
+  float* delta = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + one);
+  prm.lse2 = lse2;
+  prm.delta = delta;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.G = Hq / Hkv;
+  prm.Sq = Sq;
+  prm.Sk = Sk;
+  prm.Sq_pad = static_cast<int>(padded_rows(Sq));
+  prm.causal = causal != 0;
+  prm.diag = causal == 1 ? Sk - Sq : 0;
+  prm.n_qt = (Sq + BT - 1) / BT;
+  prm.n_kt = (Sk + BT - 1) / BT;
+  prm.BZ = B * Hkv;
+  prm.BH = B * Hq;
+  prm.n_items = 0;
+  prm.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  prm.scale = scale;
+  const auto* ob = static_cast<const __nv_bfloat16*>(o);
+  const auto* gb = static_cast<const __nv_bfloat16*>(dout);
+  return D == 128 ? launch_all<128>(tq, tk, tv, tdo, prm, ob, gb, lse, lse2, delta, g_dev_sms[dev], stream)
+                  : launch_all<64>(tq, tk, tv, tdo, prm, ob, gb, lse, lse2, delta, g_dev_sms[dev], stream);
+}
+
+const char* attn_bwd_strerror(int status) {
+  switch (status) {
+    case ATTN_OK: return "success";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_NULL_PTR: return "null pointer";
+    case ATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case ATTN_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+    case ATTN_ERR_CUDA: return cudaGetErrorString(t_last_cuda_error);
+    case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel wait ran out of time; the kernel unwound";
+    case ATTN_ERR_TENSOR_MAP: return "TMA tensor map rejected by the driver";
+    default: return "unknown status";
+  }
+}
+
+int attn_bwd_debug_status(cudaStream_t stream, int* site) {
+  if (site) *site = 0;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int value = 0;
+  e = cudaMemcpyFromSymbol(&value, g_bwd_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (value != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (site) *site = value;
+  return value == 0 ? ATTN_OK : ATTN_ERR_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"

@@ -197,6 +197,52 @@ def attn_fwd_blocksparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bloc
     return o, lse
 
 
+def bwd_workspace_size(B: int, Hq: int, Sq: int) -> int:
+    return int(load("attn_bwd").attn_bwd_workspace_size(B, Hq, Sq))
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+             dout: torch.Tensor, causal: int = 1, scale: float | None = None, dq: torch.Tensor | None = None,
+             dk: torch.Tensor | None = None, dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+             stream=None):
+    """Backward of ``attn_fwd``: ``(dq, dk, dv)`` for the upstream gradient ``dout`` of ``o``.
+
+    ``o`` and ``lse`` are the forward's outputs for the same ``q, k, v, causal, scale``.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-d bf16 CUDA tensor")
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("shape mismatch")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Sq) or not lse.is_contiguous():
+        raise ValueError("lse must be the forward's contiguous fp32 [B, Hq, Sq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = bwd_workspace_size(B, Hq, Sq)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    lib = load("attn_bwd")
+    st = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Sq, Sk, D, int(causal),
+                      ctypes.c_float(scale), workspace.data_ptr(), ws_bytes, _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, lib.attn_bwd_strerror(st).decode())
+    return dq, dk, dv
+
+
+def bwd_debug_status(stream=None) -> tuple[int, int]:
+    """Synchronise ``stream`` and read/clear the backward kernels' timeout word: ``(status, site)``."""
+    site = ctypes.c_int(0)
+    st = load("attn_bwd").attn_bwd_debug_status(_stream_handle(stream), ctypes.byref(site))
+    return st, site.value
+
+
 def debug_status(stream=None) -> tuple[int, int]:
     """Synchronise ``stream`` and read/clear the kernel's timeout word: ``(status, site)``."""
     site = ctypes.c_int(0)

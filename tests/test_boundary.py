@@ -13,7 +13,8 @@ from attention_forward_06_gb300 import build as B
 from attention_forward_06_gb300 import _lib, ops
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADERS = {"attn_fwd": "include/attn_fwd.h", "attn_probe": "include/attn_fwd_probe.h"}
+HEADERS = {"attn_fwd": "include/attn_fwd.h", "attn_bwd": "include/attn_bwd.h",
+           "attn_probe": "include/attn_fwd_probe.h"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -164,3 +165,22 @@ def test_blocksparse_invalid_arguments_before_any_device_work():
     assert args(0, 1) == ops.ATTN_ERR_NULL_PTR
     assert args(M + 2, 4) == ops.ATTN_ERR_MISALIGNED
     assert args(O, 1) == ops.ATTN_ERR_INVALID_ARG       # the mask overlaps the output
+
+
+def test_bwd_workspace_formula_and_invalid_arguments():
+    lib = _lib.load("attn_bwd")
+    for B, Hq, Sq in ((1, 1, 1), (2, 16, 2048), (3, 5, 300)):
+        one = B * Hq * (-(-Sq // 128) * 128) * 4
+        assert lib.attn_bwd_workspace_size(B, Hq, Sq) == 2 * ((one + 255) // 256 * 256)
+    W = 0x900000
+    call = lambda **kw: lib.attn_bwd(*[kw.get(n, a) for n, a in zip(
+        ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv"),
+        (0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000, 0x800000, 0x880000))],
+        1, 4, kw.get("Hkv", 2), 64, 64, kw.get("D", 128), 1, 0.1, kw.get("ws", W), 1 << 20, None)
+    assert call(D=96) == ops.ATTN_ERR_INVALID_ARG
+    assert call(Hkv=3) == ops.ATTN_ERR_INVALID_ARG
+    assert call(dq=0) == ops.ATTN_ERR_NULL_PTR
+    assert call(ws=0) == ops.ATTN_ERR_NULL_PTR
+    assert call(dk=0x800008) == ops.ATTN_ERR_MISALIGNED
+    assert call(dq=0x100000) == ops.ATTN_ERR_INVALID_ARG    # dq overlaps q
+    assert call(dv=0x800000) == ops.ATTN_ERR_INVALID_ARG    # dv overlaps dk
