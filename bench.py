@@ -376,6 +376,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         line["geomean_tflops"] = math.exp(sum(math.log(x) for x in per.values()) / len(per))
         line["geomean_pct_of_peak"] = 100.0 * line["geomean_tflops"] / peak
         line["blocksparse"] = bench_blocksparse(stream, flush, dev, min(args.steps, 10))
+        line["backward"] = bench_backward(stream, flush, dev, min(args.steps, 10))
     if world == 1 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     return line
@@ -409,6 +410,33 @@ def bench_blocksparse(stream, flush, dev, steps: int, density: float = 0.25) -> 
         flops = 4.0 * w.D * blocksparse_pairs(w, blocks)
         out[name] = {"tflops": flops / (ts * 1e-3) / 1e12, "ms": ts, "speedup_vs_dense": td / ts,
                      "marked_fraction": float(blocks.mean())}
+    return out
+
+
+def bench_backward(stream, flush, dev, steps: int) -> dict:
+    """Backward (dQ, dK, dV) of the train and gqa workloads.  FLOP convention: the five products of the
+    backward, 10*D per unmasked (row, key) pair (2.5x the forward); the kernels recompute S and dP for dQ,
+    which is extra work not counted."""
+    from attention_forward_06_gb300 import ops
+
+    peak = float(measured_peaks()[0]["bf16_tflops"])
+    out = {"flop_count": "algorithmic: 10*D per unmasked (row, key) pair"}
+    for name in ("train", "gqa"):
+        w = WORKLOADS[name]
+        q, k, v = [t.to(dev) for t in draw_workload(w)]
+        do = torch.randn(q.shape, generator=torch.Generator().manual_seed(w.seed + 5000)).to(torch.bfloat16).to(dev)
+        o, lse = ops.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, stream=stream)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(ops.bwd_workspace_size(w.B, w.Hq, w.Sq), dtype=torch.uint8, device=dev)
+
+        def fb():
+            ops.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                         stream=stream)
+
+        tb = statistics.mean(time_kernel(fb, steps, 3, flush, stream))
+        flops = 2.5 * alg_flops(w)
+        out[name] = {"tflops": flops / (tb * 1e-3) / 1e12, "ms": tb, "pct_of_peak": 100.0 * flops / (tb * 1e-3) / 1e12 / peak}
+        del q, k, v, do, o, lse, dq, dk, dv, ws
     return out
 
 
