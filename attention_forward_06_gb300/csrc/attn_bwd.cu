@@ -18,8 +18,9 @@
 //                          form, A from TMEM) accumulate in TMEM across the whole item
 //   attn_bwd_dq_kernel     one (batch, query head, 128-row tile) per item: S = Q K^T,
 //                          dP = dO V^T, dS into TMEM, dQ += dS K
-// Each kernel: warps 0-3 compute (one thread per TMEM lane), warp 4 loads with TMA,
-// warp 5 issues the tcgen05 MMAs; every wait is bounded as in the forward.
+// Each kernel: warps 0-7 compute (two threads per TMEM lane, each on half of the
+// tile's columns), warp 8 loads with TMA, warp 9 issues the tcgen05 MMAs; every wait
+// is bounded as in the forward.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,9 +38,10 @@ using namespace attn;
 namespace {
 
 constexpr int BT = 128;  // query rows / keys per tile (MMA M and N)
-constexpr int kThreads = 192;
-constexpr int kLoadWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;
+constexpr int kComputeWarps = 8;  // two per TMEM lane quarter, each on half of the columns
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kRing = 2;  // streamed tile-pair slots
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
@@ -140,7 +142,7 @@ __device__ __forceinline__ int first_qtile(const BParams& p, int j) {
 // dP^T [128,256), dV [256,256+D), dK [384,384+D); P^T and dS^T (bf16 pairs)
 // overwrite the first 64 columns of S^T and dP^T.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                          const BParams p) {
@@ -163,9 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(&st_full, 1);
-    mbar_init(&pt_full, 4 * 32);
+    mbar_init(&pt_full, kComputeWarps * 32);
     mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, 4 * 32);
+    mbar_init(&acc_empty, kComputeWarps * 32);
     mbar_init(&drain, 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -273,8 +275,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit_elect(&drain);
     warp_wait(&drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
   } else {
-    // ------------------------------------------------------------ compute (one thread per key)
-    const int quarter = warp;
+    // ------------------------------------------------------------ compute (two threads per key)
+    // Warp w serves the keys of TMEM lane quarter w % 4 and query rows 64 * (w / 4) .. + 63
+    // of each tile; its P^T and dS^T land in columns 32 * (w / 4) .. + 31, which the
+    // partner warp (same lanes, other rows) reads first: the two meet at a named barrier.
+    const int quarter = warp % 4, half = warp / 4;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t st_t = tmem + lane_off, dpt_t = tmem + lane_off + BT;
     const uint32_t dv_t = tmem + lane_off + 2 * BT, dk_t = tmem + lane_off + 3 * BT;
@@ -287,82 +292,100 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nI = p.n_qt - i0;
       const int key = j * BT + kk;
       const bool key_live = key < p.Sk;
-      __nv_bfloat16* dvrow = p.dv + (static_cast<int64_t>(z) * p.Sk + key) * D;
-      __nv_bfloat16* dkrow = p.dk + (static_cast<int64_t>(z) * p.Sk + key) * D;
+      // half 0 writes this key's dV row, half 1 its dK row
+      __nv_bfloat16* grow = (half == 0 ? p.dv : p.dk) + (static_cast<int64_t>(z) * p.Sk + key) * D;
       if (nI <= 0) {  // no query row sees this key tile: zero gradients
         if (key_live) {
-          uint4* a = reinterpret_cast<uint4*>(dvrow);
-          uint4* b2 = reinterpret_cast<uint4*>(dkrow);
+          uint4* a4 = reinterpret_cast<uint4*>(grow);
 #pragma unroll
-          for (int v4 = 0; v4 < D / 8; ++v4) a[v4] = b2[v4] = make_uint4(0u, 0u, 0u, 0u);
+          for (int v4 = 0; v4 < D / 8; ++v4) a4[v4] = make_uint4(0u, 0u, 0u, 0u);
         }
         continue;
       }
       for (int s = 0; s < G * nI; ++s, ++it, ++gs) {
         const int i = i0 + s % nI;
-        const int row0 = i * BT;
+        const int row0 = i * BT + 64 * half;  // first query row of this thread's columns
         const uint8_t* sl = ring + (it % kRing) * C::kSlotBytes;
-        const float* lse2v = reinterpret_cast<const float*>(sl + 2 * C::kTileBytes);
-        const float* deltav = lse2v + BT;
+        const float4* lse2v = reinterpret_cast<const float4*>(sl + 2 * C::kTileBytes) + 16 * half;
+        const float4* deltav = reinterpret_cast<const float4*>(sl + 2 * C::kTileBytes + C::kVecBytes) + 16 * half;
         // the slot's vectors have landed (this warp observes their copy itself), then S^T and dP^T
         ok = warp_wait(&full[it % kRing], (it / kRing) & 1, abort_v, kTimeoutNs);
         if (ok) ok = warp_wait(&st_full, gs & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
         // elements to mask: keys past Sk, and keys above the diagonal of a straddling tile
-        const bool diag_tile = p.causal && (j * BT + BT - 1 > row0 + p.diag);
-        const int first_ok_row = key - p.diag - row0;  // rows r >= this see the key (diagonal tiles)
+        const bool diag_tile = p.causal && (j * BT + BT - 1 > i * BT + p.diag);
+        const int first_ok = key - p.diag - row0;  // this thread's rows r >= first_ok see the key
+        // one 32-row chunk (local rows 32 cc .. + 31): P^T and dS^T as 16 bf16 pairs each;
+        // `signal` marks the chunk whose S^T and dP^T columns the partner warp overwrites
+        auto chunk = [&](int cc, uint32_t(&pk)[16], uint32_t(&dsk)[16], bool signal) {
+          uint32_t sv[32], dpv[32];
+          tmem_ld2x32_wait(st_t + 64 * half + 32 * cc, dpt_t + 64 * half + 32 * cc, sv, dpv);
+          if (signal) named_barrier_arrive(1 + quarter, 64);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t sv[32], dpv[32], pk[16], dsk[16];
-          tmem_ld32_wait(st_t + 32 * c4, sv);
-          tmem_ld32_wait(dpt_t + 32 * c4, dpv);
+          for (int r4 = 0; r4 < 8; ++r4) {
+            const float4 l4 = lse2v[8 * cc + r4], d4 = deltav[8 * cc + r4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dl[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pp[4], dd[4];
 #pragma unroll
-          for (int r2 = 0; r2 < 16; ++r2) {
-            const int r = 32 * c4 + 2 * r2;
-            float pp[2], dd[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const bool vis = key_live && (!diag_tile || r + h >= first_ok_row);
-              const float pr = vis ? ex2_approx(fmaf(__uint_as_float(sv[2 * r2 + h]), p.c, -lse2v[r + h])) : 0.0f;
+            for (int h = 0; h < 4; ++h) {
+              const int r = 32 * cc + 4 * r4 + h;
+              const bool vis = key_live && (!diag_tile || r >= first_ok);
+              const float pr = vis ? ex2_approx(fmaf(__uint_as_float(sv[4 * r4 + h]), p.c, -lv[h])) : 0.0f;
               pp[h] = pr;
-              dd[h] = pr * (__uint_as_float(dpv[2 * r2 + h]) - deltav[r + h]);
+              dd[h] = pr * (__uint_as_float(dpv[4 * r4 + h]) - dl[h]);
             }
-            pk[r2] = pack_bf16x2(pp[0], pp[1]);
-            dsk[r2] = pack_bf16x2(dd[0], dd[1]);
+            pk[2 * r4] = pack_bf16x2(pp[0], pp[1]);
+            pk[2 * r4 + 1] = pack_bf16x2(pp[2], pp[3]);
+            dsk[2 * r4] = pack_bf16x2(dd[0], dd[1]);
+            dsk[2 * r4 + 1] = pack_bf16x2(dd[2], dd[3]);
           }
-          tmem_st16(st_t + 16 * c4, pk);
-          tmem_st16(dpt_t + 16 * c4, dsk);
+        };
+        auto store = [&](int cc, const uint32_t(&pk)[16], const uint32_t(&dsk)[16]) {
+          tmem_st16(st_t + 32 * half + 16 * cc, pk);
+          tmem_st16(dpt_t + 32 * half + 16 * cc, dsk);
+        };
+        // P^T and dS^T of this thread's rows go to columns 32 * half .. + 31 of S^T and dP^T.
+        // Half 1's columns 32..63 hold S^T and dP^T of half 0's rows 32..63: half 0 signals
+        // once it has read them, and half 1 waits for that before its first store.  Half 0's
+        // own stores land in columns it has already read.
+        uint32_t pk[16], dsk[16];
+        if (half == 0) {
+          chunk(0, pk, dsk, false);
+          store(0, pk, dsk);
+          chunk(1, pk, dsk, true);
+          store(1, pk, dsk);
+        } else {
+          chunk(0, pk, dsk, false);
+          named_barrier_sync(1 + quarter, 64);
+          store(0, pk, dsk);
+          chunk(1, pk, dsk, false);
+          store(1, pk, dsk);
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&pt_full);
       }
       if (!ok) break;
-      // epilogue: dV and scale * dK of this key, bf16, once the item's last MMAs are done
+      // epilogue: dV (half 0) or scale * dK (half 1) of this key, bf16, once the item's MMAs are done
       ok = warp_wait(&acc_full, n_ne & 1, abort_v, kTimeoutNs);
       if (!ok) break;
       ++n_ne;
       tc_fence_after();
+      const float mul = half == 0 ? 1.0f : p.scale;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const float mul = which == 0 ? 1.0f : p.scale;
-        __nv_bfloat16* dst = which == 0 ? dvrow : dkrow;
+      for (int cb = 0; cb < D / 32; ++cb) {
+        uint32_t a[32];
+        tmem_ld32_wait((half == 0 ? dv_t : dk_t) + 32 * cb, a);
+        if (key_live) {
+          uint4* d4 = reinterpret_cast<uint4*>(grow + 32 * cb);
 #pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          uint32_t a[32];
-          tmem_ld32_wait((which == 0 ? dv_t : dk_t) + 32 * cb, a);
-          if (key_live) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cb);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t w[4];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint32_t w[4];
-#pragma unroll
-              for (int h = 0; h < 4; ++h)
-                w[h] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * h]) * mul,
-                                   __uint_as_float(a[8 * q4 + 2 * h + 1]) * mul);
-              d4[q4] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
+            for (int h = 0; h < 4; ++h)
+              w[h] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * h]) * mul, __uint_as_float(a[8 * q4 + 2 * h + 1]) * mul);
+            d4[q4] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
@@ -393,7 +416,7 @@ __device__ __forceinline__ int key_tiles(const BParams& p, int i) {
 // mask), slice bh = x % (B*Hq).  TMEM (lane = query row): S [0,128), dP [128,256),
 // dQ [256,256+D); dS (bf16 pairs) overwrites the first 64 columns of S.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                        const BParams p) {
@@ -415,9 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(&s_full, 1);
-    mbar_init(&ds_full, 4 * 32);
+    mbar_init(&ds_full, kComputeWarps * 32);
     mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, 4 * 32);
+    mbar_init(&acc_empty, kComputeWarps * 32);
     mbar_init(&drain, 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -514,8 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit_elect(&drain);
     warp_wait(&drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
   } else {
-    // ------------------------------------------------------------ compute (one thread per query row)
-    const int quarter = warp;
+    // ------------------------------------------------------------ compute (two threads per query row)
+    // Warp w serves the rows of TMEM lane quarter w % 4 and keys 64 * (w / 4) .. + 63 of
+    // each tile; its dS lands in columns 32 * (w / 4) .. + 31 (read first by the partner).
+    const int quarter = warp % 4, half = warp / 4;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_t = tmem + lane_off, dp_t = tmem + lane_off + BT, dq_t = tmem + lane_off + 2 * BT;
     uint32_t gs = 0, n_ne = 0;
@@ -525,12 +550,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = key_tiles(p, i);
       const int row = i * BT + quarter * 32 + lane;
       const bool live = row < p.Sq;
-      __nv_bfloat16* dqrow = p.dq + (static_cast<int64_t>(bh) * p.Sq + row) * D;
+      // half h writes columns h * D/2 .. of this row's dQ
+      __nv_bfloat16* dqrow = p.dq + (static_cast<int64_t>(bh) * p.Sq + row) * D + half * (D / 2);
       if (n <= 0) {  // no key is visible to any row of this tile: zero gradient
         if (live) {
-          uint4* a = reinterpret_cast<uint4*>(dqrow);
+          uint4* a4 = reinterpret_cast<uint4*>(dqrow);
 #pragma unroll
-          for (int v4 = 0; v4 < D / 8; ++v4) a[v4] = make_uint4(0u, 0u, 0u, 0u);
+          for (int v4 = 0; v4 < D / 16; ++v4) a4[v4] = make_uint4(0u, 0u, 0u, 0u);
         }
         continue;
       }
@@ -541,25 +567,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = warp_wait(&s_full, gs & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        const int kmax = lim - j * BT;  // keys of this tile past kmax are masked
+        uint32_t sv[64], dpv[64];
+        tmem_ld2x64_wait(s_t + 64 * half, dp_t + 64 * half, sv, dpv);
+        named_barrier_sync(1 + quarter, 64);  // both halves hold their S and dP columns
+        const int kmax = lim - j * BT - 64 * half;  // this thread's keys past kmax are masked
+        uint32_t dsk[32];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t sv[32], dpv[32], dsk[16];
-          tmem_ld32_wait(s_t + 32 * c4, sv);
-          tmem_ld32_wait(dp_t + 32 * c4, dpv);
+        for (int e2 = 0; e2 < 32; ++e2) {
+          float dd[2];
 #pragma unroll
-          for (int e2 = 0; e2 < 16; ++e2) {
-            float dd[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int e = 32 * c4 + 2 * e2 + h;
-              const float pr = e <= kmax ? ex2_approx(fmaf(__uint_as_float(sv[2 * e2 + h]), p.c, -lse2)) : 0.0f;
-              dd[h] = pr * (__uint_as_float(dpv[2 * e2 + h]) - delt);
-            }
-            dsk[e2] = pack_bf16x2(dd[0], dd[1]);
+          for (int h = 0; h < 2; ++h) {
+            const int e = 2 * e2 + h;
+            const float pr = e <= kmax ? ex2_approx(fmaf(__uint_as_float(sv[e]), p.c, -lse2)) : 0.0f;
+            dd[h] = pr * (__uint_as_float(dpv[e]) - delt);
           }
-          tmem_st16(s_t + 16 * c4, dsk);
+          dsk[e2] = pack_bf16x2(dd[0], dd[1]);
         }
+        tmem_st32(s_t + 32 * half, dsk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&ds_full);
@@ -570,9 +594,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n_ne;
       tc_fence_after();
 #pragma unroll
-      for (int cb = 0; cb < D / 32; ++cb) {
+      for (int cb = 0; cb < D / 64; ++cb) {
         uint32_t a[32];
-        tmem_ld32_wait(dq_t + 32 * cb, a);
+        tmem_ld32_wait(dq_t + half * (D / 2) + 32 * cb, a);
         if (live) {
           uint4* d4 = reinterpret_cast<uint4*>(dqrow + 32 * cb);
 #pragma unroll

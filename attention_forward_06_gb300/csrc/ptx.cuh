@@ -195,6 +195,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // Barrier over `count` threads (whole warps) on hardware barrier `id` (1..15; 0 is __syncthreads).
+// Signal a named barrier without waiting (the producer side of a bar.sync).
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -487,6 +492,50 @@ __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, uint32_t (&r)[12
         ATTN_R8(112), ATTN_R8(120)
       : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96)
       : "memory");
+}
+
+// Two runs of 32 consecutive columns (at a and at b), two x32 loads, one wait.
+__device__ __forceinline__ void tmem_ld2x32_wait(uint32_t ta, uint32_t tb, uint32_t (&r)[32], uint32_t (&q)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : ATTN_R8(0), ATTN_R8(8), ATTN_R8(16), ATTN_R8(24),
+        "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7]),
+        "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15]),
+        "=r"(q[16]), "=r"(q[17]), "=r"(q[18]), "=r"(q[19]), "=r"(q[20]), "=r"(q[21]), "=r"(q[22]), "=r"(q[23]),
+        "=r"(q[24]), "=r"(q[25]), "=r"(q[26]), "=r"(q[27]), "=r"(q[28]), "=r"(q[29]), "=r"(q[30]), "=r"(q[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
+// Two runs of 64 consecutive columns (at a and at b), four x32 loads, one wait.
+__device__ __forceinline__ void tmem_ld2x64_wait(uint32_t ta, uint32_t tb, uint32_t (&r)[64], uint32_t (&q)[64]) {
+#define ATTN_Q8(b) "=r"(q[b + 0]), "=r"(q[b + 1]), "=r"(q[b + 2]), "=r"(q[b + 3]), \
+                   "=r"(q[b + 4]), "=r"(q[b + 5]), "=r"(q[b + 6]), "=r"(q[b + 7])
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+      "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : ATTN_R8(0), ATTN_R8(8), ATTN_R8(16), ATTN_R8(24), ATTN_R8(32), ATTN_R8(40), ATTN_R8(48), ATTN_R8(56),
+        ATTN_Q8(0), ATTN_Q8(8), ATTN_Q8(16), ATTN_Q8(24), ATTN_Q8(32), ATTN_Q8(40), ATTN_Q8(48), ATTN_Q8(56)
+      : "r"(ta), "r"(ta + 32), "r"(tb), "r"(tb + 32)
+      : "memory");
+#undef ATTN_Q8
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
