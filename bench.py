@@ -377,6 +377,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         line["geomean_pct_of_peak"] = 100.0 * line["geomean_tflops"] / peak
         line["blocksparse"] = bench_blocksparse(stream, flush, dev, min(args.steps, 10))
         line["backward"] = bench_backward(stream, flush, dev, min(args.steps, 10))
+        line["splitkv"] = bench_splitkv(stream, flush, dev, min(args.steps, 10))
     if world == 1 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     return line
@@ -411,6 +412,34 @@ def bench_blocksparse(stream, flush, dev, steps: int, density: float = 0.25) -> 
         out[name] = {"tflops": flops / (ts * 1e-3) / 1e12, "ms": ts, "speedup_vs_dense": td / ts,
                      "marked_fraction": float(blocks.mean())}
     return out
+
+
+def bench_splitkv(stream, flush, dev, steps: int) -> dict:
+    """Split-key forward on a shape with too few work items for the GPU -- one 512-row chunk of 32 query heads
+    (8 kv heads) over 131072 keys, bottom-right causal, N(0,1) -- against the plain forward."""
+    from attention_forward_06_gb300 import ops
+    import dataclasses
+
+    w = dataclasses.replace(WORKLOADS["chunked128"], name="splitkv_probe", B=1, Sq=512, Sk=131072, seed=6)
+    qx, kx, vx = [t.to(dev) for t in draw_workload(w)]
+    ox = torch.empty_like(qx)
+    lx = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    n_splits = ops.splitkv_suggest(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal)
+    ws = torch.empty(ops.splitkv_workspace_size(w.B, w.Hq, w.Sq, w.D, n_splits), dtype=torch.uint8, device=dev)
+
+    def fp():
+        ops.attn_fwd(qx, kx, vx, causal=w.causal, scale=w.scale, o=ox, lse=lx, stream=stream)
+
+    def fs():
+        ops.attn_fwd_splitkv(qx, kx, vx, causal=w.causal, scale=w.scale, n_splits=n_splits, workspace=ws, o=ox,
+                             lse=lx, stream=stream)
+
+    tp = statistics.mean(time_kernel(fp, steps, 3, flush, stream))
+    ts = statistics.mean(time_kernel(fs, steps, 3, flush, stream))
+    flops = alg_flops(w)
+    return {"workload": f"{w.label()} (a prefill chunk over a long context)", "n_splits": n_splits,
+            "tflops": flops / (ts * 1e-3) / 1e12, "ms": ts, "plain_ms": tp,
+            "plain_tflops": flops / (tp * 1e-3) / 1e12, "speedup_vs_plain": tp / ts}
 
 
 def bench_backward(stream, flush, dev, steps: int) -> dict:
