@@ -442,7 +442,7 @@ def bench_splitkv(stream, flush, dev, steps: int) -> dict:
             "plain_tflops": flops / (tp * 1e-3) / 1e12, "speedup_vs_plain": tp / ts}
 
 
-def bench_backward(stream, flush, dev, steps: int) -> dict:
+def bench_backward(stream, flush, dev, steps: int, names=("train", "gqa"), warmup: int = 3) -> dict:
     """Backward (dQ, dK, dV) of the train and gqa workloads.  FLOP convention: the five products of the
     backward, 10*D per unmasked (row, key) pair (2.5x the forward); the kernels recompute S and dP for dQ,
     which is extra work not counted."""
@@ -450,7 +450,7 @@ def bench_backward(stream, flush, dev, steps: int) -> dict:
 
     peak = float(measured_peaks()[0]["bf16_tflops"])
     out = {"flop_count": "algorithmic: 10*D per unmasked (row, key) pair"}
-    for name in ("train", "gqa"):
+    for name in names:
         w = WORKLOADS[name]
         q, k, v = [t.to(dev) for t in draw_workload(w)]
         do = torch.randn(q.shape, generator=torch.Generator().manual_seed(w.seed + 5000)).to(torch.bfloat16).to(dev)
@@ -462,7 +462,7 @@ def bench_backward(stream, flush, dev, steps: int) -> dict:
             ops.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
                          stream=stream)
 
-        tb = statistics.mean(time_kernel(fb, steps, 3, flush, stream))
+        tb = statistics.mean(time_kernel(fb, steps, warmup, flush, stream))
         flops = 2.5 * alg_flops(w)
         out[name] = {"tflops": flops / (tb * 1e-3) / 1e12, "ms": tb, "pct_of_peak": 100.0 * flops / (tb * 1e-3) / 1e12 / peak}
         del q, k, v, do, o, lse, dq, dk, dv, ws
@@ -478,6 +478,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-workloads", action="store_true", help="time only --workload, not the geomean set")
+    ap.add_argument("--backward", action="store_true",
+                    help="time only the backward (attn_bwd) of --workload and print its own JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -494,6 +496,16 @@ def main():
             tdist.init_process_group("nccl")
             dist = tdist
     w = WORKLOADS[args.workload]
+    if args.backward:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py --backward needs a GPU (the CUDA path has no CPU fallback)")
+        dev = torch.device("cuda", torch.cuda.current_device())
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        res = bench_backward(torch.cuda.current_stream(dev), flush, dev, args.steps, names=(w.name,),
+                             warmup=args.warmup)
+        print(json.dumps({"metric": "attn bwd TFLOPS (bf16, 1xGB300), 10*D FLOP per unmasked pair",
+                          "workload": w.label(), "steps": args.steps, "warmup": args.warmup, **res[w.name]}))
+        return 0
     if args.impl == "reference":
         line = run_reference(args, w, rank, world)
     else:
