@@ -5,16 +5,17 @@
 //
 // Persistent kernel: one CTA per SM walks a list of work items, each 256 query
 // rows (two 128-row Q tiles) of one (batch, query head).  Items are ordered
-// heaviest first (most key tiles under a causal mask) and dealt to the CTAs in
-// a boustrophedon order (0..G-1, then G-1..0, ...) so every CTA gets a similar
-// amount of work.  Twelve warps:
+// heaviest first (most key tiles under a causal mask); CTA c starts on item c
+// and claims later items from a counter as it frees up, so the CTAs end within
+// about one small item of each other.  Twelve warps:
 //   warps 0-3   softmax for Q tile 0 (one thread per query row), then its epilogue
 //   warps 4-7   softmax for Q tile 1, then its epilogue
 //   warp  8     TMA producer: the Q tiles of an item, then its K/V tiles through a
 //               ring of shared-memory slots guarded by full/empty mbarriers
 //   warp  9     tcgen05 issuer: S_t = Q_t K^T into tensor memory (TMEM), and
 //               O_t += P_t V with P_t read back from TMEM; owns the TMEM allocation
-//   warps 10-11 idle (they complete the third warpgroup)
+//   warp  10    idle (it completes the third warpgroup)
+//   warp  11    TMA stores of O once the softmax warps have staged it
 // Registers are rebalanced per warpgroup after set-up: the softmax warpgroups
 // grow to 224 per thread (a whole S row lives in registers), the third shrinks
 // to 56; 128*56 + 256*224 equals the 384*168 the block is launched with.
@@ -219,11 +220,13 @@ __device__ int g_status;  // sticky: 0 = fine, else the site of the first wait t
 // Dynamic schedule.  CTA c starts on item c; later items are claimed in list
 // order (heaviest first) from a counter, so a CTA that finishes early takes the
 // next item and the CTAs end within about one (small) item of each other.  Each
-// launch uses one of kSchedSlots counter pairs (claimed items, CTAs finished),
-// chosen by the host; the last CTA to finish returns its pair to zero.
+// launch uses one of kSchedSlots counters, chosen by the host in turn.  Every CTA
+// claims until a claim comes back past the last item, so a launch makes exactly
+// n_items claims (a CTA that unwinds early makes the rest of its claims before it
+// exits); the claim numbered n_items - 1 is the launch's last, and its taker
+// returns the counter to zero, with no end-of-kernel synchronisation.
 constexpr int kSchedSlots = 64;
 __device__ int g_sched_next[kSchedSlots];
-__device__ unsigned int g_sched_done[kSchedSlots];
 constexpr int kSeqSlots = 4;  // depth of the shared-memory ring through which the producer publishes items
 constexpr int kSeqConsumers = 10;  // warps reading the ring: eight softmax warps, the issuer, the store warp
 
@@ -356,7 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // key tiles before its end), so items are handed out in the order CTAs free up.
       auto claim = [&]() {
         int claimed = 0;
-        if (lane == 0) claimed = atomicAdd(&g_sched_next[p.sched_slot], 1);
+        if (lane == 0) {
+          claimed = atomicAdd(&g_sched_next[p.sched_slot], 1);
+          if (claimed == p.n_items - 1) g_sched_next[p.sched_slot] = 0;  // the launch's last claim
+        }
         return static_cast<int>(gridDim.x) + __shfl_sync(0xffffffffu, claimed, 0);
       };
       if (n_tiles == 0) {
@@ -418,7 +424,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) x = claim();
     }
     if (!ok) {
-      if (lane == 0) record_abort(abort_v, kSiteProducer);
+      if (lane == 0) {
+        record_abort(abort_v, kSiteProducer);
+        // the claims this CTA has not made yet, up to its first one past the last item,
+        // so the launch still makes n_items claims and its last taker resets the counter
+        while (x < p.n_items) {
+          const int claimed = atomicAdd(&g_sched_next[p.sched_slot], 1);
+          if (claimed == p.n_items - 1) g_sched_next[p.sched_slot] = 0;
+          x = static_cast<int>(gridDim.x) + claimed;
+        }
+      }
       // unwinding: let the copies already in flight land before the CTA exits
       if (q_issued > 0) mbar_wait_bounded(&q_full, (q_issued - 1) & 1, abort_v, kDrainTimeoutNs);
       for (uint32_t i = (kv_it > S ? kv_it - S : 0); i < kv_it; ++i)
@@ -850,14 +865,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
-  }
-  if (threadIdx.x == 0) {  // every claim of this CTA is done; the last CTA resets the counters
-    __threadfence();
-    if (atomicAdd(&g_sched_done[p.sched_slot], 1u) == gridDim.x - 1) {
-      g_sched_next[p.sched_slot] = 0;
-      g_sched_done[p.sched_slot] = 0;
-      __threadfence();
-    }
   }
 }
 

@@ -153,3 +153,56 @@ def test_wrong_dtype_is_rejected_by_binding():
     q, k, v = [t.cuda() for t in draw(1, 1, 1, 16, 16, 64, seed=11)]
     with pytest.raises(ValueError):
         ops.attn_fwd(q.float(), k, v)
+
+
+def test_schedule_counters_across_many_launches():
+    """Each launch claims work items from one of a set of device counters, and the
+    launch's last claim returns its counter to zero.  Many launches in a row, on two
+    streams and with item counts below and above the SM count, mixing the plain,
+    split-key and block-sparse entry points, must each reproduce the first result
+    bit for bit (a counter left non-zero would skip items and leave NaN behind)."""
+    dev = torch.device("cuda")
+    cases = []
+    for (B, Hq, Hkv, Sq, Sk, D, causal) in [(2, 16, 4, 2048, 2048, 128, 1), (1, 4, 4, 1000, 1000, 64, 0),
+                                            (1, 2, 1, 300, 4000, 128, 1)]:
+        q, k, v = (t.to(dev) for t in draw(B, Hq, Hkv, Sq, Sk, D, seed=Sq + Sk))
+        cases.append((q, k, v, causal))
+    mask_q, mask_k, mask_v, _ = cases[0]
+    gen = torch.Generator().manual_seed(7)
+    blocks = (torch.rand(2, 1, 16, 16, generator=gen) < 0.4) | torch.eye(16, dtype=torch.bool)
+    mask = ops.pack_block_mask(blocks).to(dev)
+
+    def call(i, stream):
+        q, k, v, causal = cases[i % 3]
+        kind = (i // 3) % 3
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full(q.shape[:3], float("nan"), device=dev)
+        if kind == 0:
+            ops.attn_fwd(q, k, v, causal=causal, o=o, lse=lse, stream=stream)
+        elif kind == 1:
+            ops.attn_fwd_splitkv(q, k, v, causal=causal, n_splits=3, o=o, lse=lse, stream=stream)
+        else:
+            q, k, v, causal = mask_q, mask_k, mask_v, 1
+            o = torch.full_like(q, float("nan"))
+            lse = torch.full(q.shape[:3], float("nan"), device=dev)
+            ops.attn_fwd_blocksparse(q, k, v, mask, causal=causal, o=o, lse=lse, stream=stream)
+        return (i % 3, kind), o, lse
+
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    first = {}
+    results = []
+    for i in range(150):
+        s = streams[i % 2]
+        with torch.cuda.stream(s):
+            results.append(call(i, s))
+        if i % 10 == 9:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    st, site = ops.debug_status()
+    assert st == ops.ATTN_OK, f"kernel wait ran out at site {site}"
+    for key, o, lse in results:
+        if key not in first:
+            first[key] = (o, lse)
+            assert not torch.isnan(o.float()).any() and not torch.isnan(lse).any(), key
+        else:
+            assert torch.equal(o, first[key][0]) and torch.equal(lse, first[key][1]), key
