@@ -37,11 +37,17 @@ using namespace attn;
 
 namespace {
 
-constexpr int BT = 128;  // query rows / keys per tile (MMA M and N)
-constexpr int kThreads = 320;
-constexpr int kComputeWarps = 8;  // two per TMEM lane quarter, each on half of the columns
+constexpr int BT = 128;  // query rows / keys per tile (MMA M)
+constexpr int BH2 = 64;  // rows (dK/dV) or keys (dQ) of one half step (MMA N of the S-type products)
+constexpr int kHalfBytes = BH2 * 128;  // byte offset of a tile's second half of rows in a 128-B-swizzled block
+constexpr int kThreads = 384;          // three warpgroups
+constexpr int kComputeWarps = 8;       // warpgroup r computes half r of every step
 constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;            // warps 10 and 11 idle (they complete the third warpgroup)
+constexpr uint32_t kRegsLaunch = 168;   // 65536 / 384
+constexpr uint32_t kRegsCompute = 224;  // warpgroups 0 and 1
+constexpr uint32_t kRegsOther = 56;     // warpgroup 2
+static_assert(256 * kRegsCompute + 128 * kRegsOther <= kThreads * kRegsLaunch, "register split exceeds the pool");
 constexpr int kRing = 2;  // streamed tile-pair slots
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
@@ -138,11 +144,16 @@ __device__ __forceinline__ int first_qtile(const BParams& p, int j) {
 
 // ---------------------------------------------------------------------------- dK, dV
 // Work item x: key tile j = x / (B*Hkv) (ascending: under a causal mask the
-// heaviest first), kv slice z = x % (B*Hkv).  TMEM (lane = key): S^T [0,128),
-// dP^T [128,256), dV [256,256+D), dK [384,384+D); P^T and dS^T (bf16 pairs)
-// overwrite the first 64 columns of S^T and dP^T.
+// heaviest first), kv slice z = x % (B*Hkv).  A step is one 128-row query tile of
+// one query head of the group, taken in two halves of 64 rows; half r lives in
+// TMEM region r (lane = key): S^T_r at columns [128 r, 128 r + 64), dP^T_r at
+// [128 r + 64, 128 r + 128), and P^T_r, dS^T_r (bf16 pairs) are written over the
+// first 32 columns of each.  dV [256, 256 + D) and dK [384, 384 + D) accumulate
+// over the whole item.  Compute warpgroup r owns half r, so one half's
+// exponentials run while the tensor cores work on the other half:
+//   S_0(s) S_1(s) | dVdK_0(s) S_0(s+1) dVdK_1(s) S_1(s+1) | ...
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                          const BParams p) {
@@ -152,7 +163,8 @@ __global__ void __maxnreg__(200)
   uint8_t* k_s = smem;
   uint8_t* v_s = smem + C::kTileBytes;
   uint8_t* ring = smem + 2 * C::kTileBytes;  // slot: Q, dO, lse2[128], delta[128]
-  __shared__ uint64_t kv_full, kv_empty, full[kRing], empty[kRing], st_full, pt_full, acc_full, acc_empty, drain;
+  __shared__ uint64_t kv_full, kv_empty, full[kRing], empty[kRing], st_full[2], pt_full[2], acc_full, acc_empty,
+      drain;
   __shared__ uint32_t tmem_slot, abort_flag;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int nz = p.BZ;
@@ -164,8 +176,10 @@ __global__ void __maxnreg__(200)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(&st_full, 1);
-    mbar_init(&pt_full, kComputeWarps * 32);
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&st_full[r], 1);
+      mbar_init(&pt_full[r], 128);
+    }
     mbar_init(&acc_full, 1);
     mbar_init(&acc_empty, kComputeWarps * 32);
     mbar_init(&drain, 1);
@@ -183,7 +197,9 @@ __global__ void __maxnreg__(200)
   volatile uint32_t* abort_v = &abort_flag;
   const int G = p.G;
 
-  if (warp == kLoadWarp) {
+  if (warp >= 8) {
+   regs_decrease<kRegsOther>();
+   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
     uint32_t it = 0, n_ne = 0;  // ring loads issued; items with query tiles
     bool ok = true;
@@ -226,46 +242,67 @@ __global__ void __maxnreg__(200)
         mbar_wait_bounded(&full[u % kRing], (u / kRing) & 1, abort_v, kDrainTimeoutNs);
       if (n_ne > 0) mbar_wait_bounded(&kv_full, (n_ne - 1) & 1, abort_v, kDrainTimeoutNs);
     }
-  } else if (warp == kMmaWarp) {
+   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tcgen05 issuer
-    const uint32_t idesc_s = idesc_bf16_f32(BT, BT, false);
-    const uint32_t idesc_acc = idesc_bf16_f32(BT, D, true);
+    constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BH2, false);  // M = 128 keys, N = 64 query rows
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(BT, D, true);   // M = 128 keys, N = D, B MN-major
     const uint32_t k_addr = smem_u32(k_s), v_addr = smem_u32(v_s), ring_addr = smem_u32(ring);
-    uint32_t it = 0, gs = 0, n_ne = 0;  // ring uses, steps (st/pt phases), items with query tiles
+    // S^T_r = K Q_r^T and dP^T_r = V dO_r^T for half r of the query tile in ring slot `slot`
+    // (K steps over D; a half starts 64 rows = kHalfBytes into each 64-column block)
+    auto issue_s = [&](int r, uint32_t slot) {
+      const uint32_t q_addr = opaque(ring_addr) + slot * C::kSlotBytes + r * kHalfBytes;
+      const uint64_t kd = sdesc_sw128(k_addr, 16, 1024), vd = sdesc_sw128(v_addr, 16, 1024);
+      const uint64_t qd = sdesc_sw128(q_addr, 16, 1024), dod = sdesc_sw128(q_addr + C::kTileBytes, 16, 1024);
+      if constexpr (D == 128) {
+        mma_bf16_ss_k8(tmem + 128 * r, kd, qd, idesc_s);
+        mma_bf16_ss_k8(tmem + 128 * r + BH2, vd, dod, idesc_s, smem_u32(&st_full[r]));
+      } else {
+        mma_bf16_ss_k4(tmem + 128 * r, kd, qd, idesc_s);
+        mma_bf16_ss_k4(tmem + 128 * r + BH2, vd, dod, idesc_s, smem_u32(&st_full[r]));
+      }
+    };
+    // dV += P^T_r dO_r and dK += dS^T_r Q_r: A from TMEM (K = the half's 64 rows), B (dO, Q)
+    // MN-major over those rows
+    auto issue_acc = [&](int r, uint32_t slot, uint32_t acc, uint32_t bar0, uint32_t bar1) {
+      const uint32_t q_addr = opaque(ring_addr) + slot * C::kSlotBytes + r * kHalfBytes;
+      const uint64_t dob = sdesc_sw128(q_addr + C::kTileBytes, C::kColBlockBytes, 1024);
+      const uint64_t qb = sdesc_sw128(q_addr, C::kColBlockBytes, 1024);
+      mma_bf16_ts_k4(tmem + 2 * BT, tmem + 128 * r, dob, idesc_acc, acc);
+      mma_bf16_ts_k4(tmem + 3 * BT, tmem + 128 * r + BH2, qb, idesc_acc, acc, bar0, bar1);
+    };
+    uint32_t it = 0, g = 0, n_ne = 0;  // ring uses, steps (st/pt phases), items with query tiles
     bool ok = true;
     for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
       const int j = x / nz;
       const int nI = p.n_qt - first_qtile(p, j);
       if (nI <= 0) continue;
+      const int T = G * nI;  // steps of the item
       ok = warp_wait(&kv_full, n_ne & 1, abort_v, kTimeoutNs);
+      if (ok) ok = warp_wait(&full[it % kRing], (it / kRing) & 1, abort_v, kTimeoutNs);
       if (!ok) break;
-      const uint64_t kd = sdesc_sw128(k_addr, 16, 1024), vd = sdesc_sw128(v_addr, 16, 1024);
-      for (int s = 0; s < G * nI; ++s, ++it, ++gs) {
-        const uint32_t slot = it % kRing;
-        const uint32_t q_addr = opaque(ring_addr) + slot * C::kSlotBytes;
-        const uint32_t do_addr = q_addr + C::kTileBytes;
-        ok = warp_wait(&full[slot], (it / kRing) & 1, abort_v, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T (keys in the TMEM lanes), K steps over D
-        const uint64_t qd = sdesc_sw128(q_addr, 16, 1024), dod = sdesc_sw128(do_addr, 16, 1024);
-        if constexpr (D == 128) {
-          mma_bf16_ss_k8(tmem, kd, qd, idesc_s);
-          mma_bf16_ss_k8(tmem + BT, vd, dod, idesc_s, smem_u32(&st_full));
-        } else {
-          mma_bf16_ss_k4(tmem, kd, qd, idesc_s);
-          mma_bf16_ss_k4(tmem + BT, vd, dod, idesc_s, smem_u32(&st_full));
-        }
-        ok = warp_wait(&pt_full, gs & 1, abort_v, kTimeoutNs);
+      tc_fence_after();
+      issue_s(0, it % kRing);
+      issue_s(1, it % kRing);
+      for (int s = 0; s < T; ++s, ++it, ++g) {
+        const uint32_t slot = it % kRing, next = (it + 1) % kRing;
+        const bool more = s + 1 < T;
+        ok = warp_wait(&pt_full[0], g & 1, abort_v, kTimeoutNs);
         if (ok && s == 0 && n_ne > 0) ok = warp_wait(&acc_empty, (n_ne - 1) & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        // dV += P^T dO and dK += dS^T Q: A from TMEM, B (dO, Q) MN-major over the query rows
-        const uint64_t dob = sdesc_sw128(do_addr, C::kColBlockBytes, 1024);
-        const uint64_t qb = sdesc_sw128(q_addr, C::kColBlockBytes, 1024);
-        mma_bf16_ts_k8(tmem + 2 * BT, tmem, dob, idesc_acc, s > 0 ? 1u : 0u);
-        mma_bf16_ts_k8(tmem + 3 * BT, tmem + BT, qb, idesc_acc, s > 0 ? 1u : 0u, smem_u32(&empty[slot]),
-                       s + 1 == G * nI ? smem_u32(&acc_full) : kNoBar);
+        issue_acc(0, slot, s > 0 ? 1u : 0u, kNoBar, kNoBar);
+        if (more) {
+          ok = warp_wait(&full[next], ((it + 1) / kRing) & 1, abort_v, kTimeoutNs);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(0, next);  // region 0 is free once the MMAs just issued have read it
+        }
+        ok = warp_wait(&pt_full[1], g & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        // half 1's products are the slot's last readers; the item's last one completes dV and dK
+        issue_acc(1, slot, 1u, smem_u32(&empty[slot]), more ? kNoBar : smem_u32(&acc_full));
+        if (more) issue_s(1, next);
       }
       if (!ok) break;
       mma_commit_elect(&kv_empty);  // K and V of this item are no longer read
@@ -274,17 +311,20 @@ __global__ void __maxnreg__(200)
     if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
     mma_commit_elect(&drain);
     warp_wait(&drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
+   }
   } else {
-    // ------------------------------------------------------------ compute (two threads per key)
-    // Warp w serves the keys of TMEM lane quarter w % 4 and query rows 64 * (w / 4) .. + 63
-    // of each tile; its P^T and dS^T land in columns 32 * (w / 4) .. + 31, which the
-    // partner warp (same lanes, other rows) reads first: the two meet at a named barrier.
-    const int quarter = warp % 4, half = warp / 4;
+    // ------------------------------------------------------------ compute (one thread per key)
+    // Warpgroup r takes half r (query rows 64 r .. 64 r + 63) of every step: the thread of
+    // key kk reads its lane of S^T_r and dP^T_r (64 columns each) and writes P^T_r and
+    // dS^T_r over their first 32 columns, its own lane only.  At the end of an item
+    // warpgroup 0 writes dV, warpgroup 1 scale * dK.
+    regs_increase<kRegsCompute>();
+    const int r = warp / 4, quarter = warp % 4;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t st_t = tmem + lane_off, dpt_t = tmem + lane_off + BT;
-    const uint32_t dv_t = tmem + lane_off + 2 * BT, dk_t = tmem + lane_off + 3 * BT;
+    const uint32_t st_t = tmem + lane_off + 128 * r, dpt_t = st_t + BH2;
+    const uint32_t acc_t = tmem + lane_off + (r == 0 ? 2 * BT : 3 * BT);
     const int kk = quarter * 32 + lane;
-    uint32_t it = 0, gs = 0, n_ne = 0;
+    uint32_t it = 0, g = 0, n_ne = 0;
     bool ok = true;
     for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
       const int j = x / nz, z = x % nz;
@@ -292,8 +332,7 @@ __global__ void __maxnreg__(200)
       const int nI = p.n_qt - i0;
       const int key = j * BT + kk;
       const bool key_live = key < p.Sk;
-      // half 0 writes this key's dV row, half 1 its dK row
-      __nv_bfloat16* grow = (half == 0 ? p.dv : p.dk) + (static_cast<int64_t>(z) * p.Sk + key) * D;
+      __nv_bfloat16* grow = (r == 0 ? p.dv : p.dk) + (static_cast<int64_t>(z) * p.Sk + key) * D;
       if (nI <= 0) {  // no query row sees this key tile: zero gradients
         if (key_live) {
           uint4* a4 = reinterpret_cast<uint4*>(grow);
@@ -302,81 +341,58 @@ __global__ void __maxnreg__(200)
         }
         continue;
       }
-      for (int s = 0; s < G * nI; ++s, ++it, ++gs) {
+      for (int s = 0; s < G * nI; ++s, ++it, ++g) {
         const int i = i0 + s % nI;
-        const int row0 = i * BT + 64 * half;  // first query row of this thread's columns
         const uint8_t* sl = ring + (it % kRing) * C::kSlotBytes;
-        const float4* lse2v = reinterpret_cast<const float4*>(sl + 2 * C::kTileBytes) + 16 * half;
-        const float4* deltav = reinterpret_cast<const float4*>(sl + 2 * C::kTileBytes + C::kVecBytes) + 16 * half;
-        // the slot's vectors have landed (this warp observes their copy itself), then S^T and dP^T
+        const float4* lse2v = reinterpret_cast<const float4*>(sl + 2 * C::kTileBytes) + (BH2 / 4) * r;
+        const float4* deltav = reinterpret_cast<const float4*>(sl + 2 * C::kTileBytes + C::kVecBytes) + (BH2 / 4) * r;
+        // the slot's vectors have landed (this warp observes their copy itself), then S^T_r and dP^T_r
         ok = warp_wait(&full[it % kRing], (it / kRing) & 1, abort_v, kTimeoutNs);
-        if (ok) ok = warp_wait(&st_full, gs & 1, abort_v, kTimeoutNs);
+        if (ok) ok = warp_wait(&st_full[r], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
         // elements to mask: keys past Sk, and keys above the diagonal of a straddling tile
         const bool diag_tile = p.causal && (j * BT + BT - 1 > i * BT + p.diag);
-        const int first_ok = key - p.diag - row0;  // this thread's rows r >= first_ok see the key
-        // one 32-row chunk (local rows 32 cc .. + 31): P^T and dS^T as 16 bf16 pairs each;
-        // `signal` marks the chunk whose S^T and dP^T columns the partner warp overwrites
-        auto chunk = [&](int cc, uint32_t(&pk)[16], uint32_t(&dsk)[16], bool signal) {
-          uint32_t sv[32], dpv[32];
-          tmem_ld2x32_wait(st_t + 64 * half + 32 * cc, dpt_t + 64 * half + 32 * cc, sv, dpv);
-          if (signal) named_barrier_arrive(1 + quarter, 64);
+        const int first_ok = key - p.diag - i * BT - BH2 * r;  // this half's rows e >= first_ok see the key
+        uint32_t sv[64], dpv[64];
+        tmem_ld2x64_wait(st_t, dpt_t, sv, dpv);
+        uint32_t pk[32], dsk[32];
 #pragma unroll
-          for (int r4 = 0; r4 < 8; ++r4) {
-            const float4 l4 = lse2v[8 * cc + r4], d4 = deltav[8 * cc + r4];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dl[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pp[4], dd[4];
+        for (int r4 = 0; r4 < 16; ++r4) {
+          const float4 l4 = lse2v[r4], d4 = deltav[r4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dl[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pp[4], dd[4];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const int r = 32 * cc + 4 * r4 + h;
-              const bool vis = key_live && (!diag_tile || r >= first_ok);
-              const float pr = vis ? ex2_approx(fmaf(__uint_as_float(sv[4 * r4 + h]), p.c, -lv[h])) : 0.0f;
-              pp[h] = pr;
-              dd[h] = pr * (__uint_as_float(dpv[4 * r4 + h]) - dl[h]);
-            }
-            pk[2 * r4] = pack_bf16x2(pp[0], pp[1]);
-            pk[2 * r4 + 1] = pack_bf16x2(pp[2], pp[3]);
-            dsk[2 * r4] = pack_bf16x2(dd[0], dd[1]);
-            dsk[2 * r4 + 1] = pack_bf16x2(dd[2], dd[3]);
+          for (int h = 0; h < 4; ++h) {
+            const int e = 4 * r4 + h;
+            const bool vis = key_live && (!diag_tile || e >= first_ok);
+            const float pr = vis ? ex2_approx(fmaf(__uint_as_float(sv[e]), p.c, -lv[h])) : 0.0f;
+            pp[h] = pr;
+            dd[h] = pr * (__uint_as_float(dpv[e]) - dl[h]);
           }
-        };
-        auto store = [&](int cc, const uint32_t(&pk)[16], const uint32_t(&dsk)[16]) {
-          tmem_st16(st_t + 32 * half + 16 * cc, pk);
-          tmem_st16(dpt_t + 32 * half + 16 * cc, dsk);
-        };
-        // P^T and dS^T of this thread's rows go to columns 32 * half .. + 31 of S^T and dP^T.
-        // Half 1's columns 32..63 hold S^T and dP^T of half 0's rows 32..63: half 0 signals
-        // once it has read them, and half 1 waits for that before its first store.  Half 0's
-        // own stores land in columns it has already read.
-        uint32_t pk[16], dsk[16];
-        if (half == 0) {
-          chunk(0, pk, dsk, false);
-          store(0, pk, dsk);
-          chunk(1, pk, dsk, true);
-          store(1, pk, dsk);
-        } else {
-          chunk(0, pk, dsk, false);
-          named_barrier_sync(1 + quarter, 64);
-          store(0, pk, dsk);
-          chunk(1, pk, dsk, false);
-          store(1, pk, dsk);
+          pk[2 * r4] = pack_bf16x2(pp[0], pp[1]);
+          pk[2 * r4 + 1] = pack_bf16x2(pp[2], pp[3]);
+          dsk[2 * r4] = pack_bf16x2(dd[0], dd[1]);
+          dsk[2 * r4 + 1] = pack_bf16x2(dd[2], dd[3]);
         }
+        tmem_st32(st_t, pk);
+        tmem_st32(dpt_t, dsk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&pt_full);
+        mbar_arrive(&pt_full[r]);
       }
       if (!ok) break;
-      // epilogue: dV (half 0) or scale * dK (half 1) of this key, bf16, once the item's MMAs are done
+      // epilogue: dV (warpgroup 0) or scale * dK (warpgroup 1) of this key, bf16, once the
+      // item's MMAs are done
       ok = warp_wait(&acc_full, n_ne & 1, abort_v, kTimeoutNs);
       if (!ok) break;
       ++n_ne;
       tc_fence_after();
-      const float mul = half == 0 ? 1.0f : p.scale;
+      const float mul = r == 0 ? 1.0f : p.scale;
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
         uint32_t a[32];
-        tmem_ld32_wait((half == 0 ? dv_t : dk_t) + 32 * cb, a);
+        tmem_ld32_wait(acc_t + 32 * cb, a);
         if (key_live) {
           uint4* d4 = reinterpret_cast<uint4*>(grow + 32 * cb);
 #pragma unroll
@@ -413,10 +429,13 @@ __device__ __forceinline__ int key_tiles(const BParams& p, int i) {
 
 // ---------------------------------------------------------------------------- dQ
 // Work item x: query tile i = n_qt - 1 - x / (B*Hq) (heaviest first under a causal
-// mask), slice bh = x % (B*Hq).  TMEM (lane = query row): S [0,128), dP [128,256),
-// dQ [256,256+D); dS (bf16 pairs) overwrites the first 64 columns of S.
+// mask), slice bh = x % (B*Hq).  A step is one 128-key tile, taken in two halves of
+// 64 keys; half r lives in TMEM region r (lane = query row): S_r at columns
+// [128 r, 128 r + 64), dP_r at [128 r + 64, 128 r + 128), dS_r (bf16 pairs) over the
+// first 32 columns of S_r; dQ [256, 256 + D) accumulates over the item.  Compute
+// warpgroup r owns half r, as in the dK/dV kernel.
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                        const BParams p) {
@@ -426,7 +445,8 @@ __global__ void __maxnreg__(200)
   uint8_t* q_s = smem;
   uint8_t* do_s = smem + C::kTileBytes;
   uint8_t* ring = smem + 2 * C::kTileBytes;  // slot: K, V
-  __shared__ uint64_t qd_full, qd_empty, full[kRing], empty[kRing], s_full, ds_full, acc_full, acc_empty, drain;
+  __shared__ uint64_t qd_full, qd_empty, full[kRing], empty[kRing], st_full[2], ds_full[2], acc_full, acc_empty,
+      drain;
   __shared__ uint32_t tmem_slot, abort_flag;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -437,8 +457,10 @@ __global__ void __maxnreg__(200)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(&s_full, 1);
-    mbar_init(&ds_full, kComputeWarps * 32);
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&st_full[r], 1);
+      mbar_init(&ds_full[r], 128);
+    }
     mbar_init(&acc_full, 1);
     mbar_init(&acc_empty, kComputeWarps * 32);
     mbar_init(&drain, 1);
@@ -455,7 +477,9 @@ __global__ void __maxnreg__(200)
   const uint32_t tmem = tmem_slot;
   volatile uint32_t* abort_v = &abort_flag;
 
-  if (warp == kLoadWarp) {
+  if (warp >= 8) {
+   regs_decrease<kRegsOther>();
+   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
     uint32_t it = 0, n_ne = 0;
     bool ok = true;
@@ -492,42 +516,60 @@ __global__ void __maxnreg__(200)
         mbar_wait_bounded(&full[u % kRing], (u / kRing) & 1, abort_v, kDrainTimeoutNs);
       if (n_ne > 0) mbar_wait_bounded(&qd_full, (n_ne - 1) & 1, abort_v, kDrainTimeoutNs);
     }
-  } else if (warp == kMmaWarp) {
+   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tcgen05 issuer
-    const uint32_t idesc_s = idesc_bf16_f32(BT, BT, false);
-    const uint32_t idesc_acc = idesc_bf16_f32(BT, D, true);
-    const uint64_t qd = sdesc_sw128(smem_u32(q_s), 16, 1024), dod = sdesc_sw128(smem_u32(do_s), 16, 1024);
-    const uint32_t ring_addr = smem_u32(ring);
-    uint32_t it = 0, gs = 0, n_ne = 0;
+    constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BH2, false);  // M = 128 rows, N = 64 keys
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(BT, D, true);   // M = 128 rows, N = D, B MN-major
+    const uint32_t q_addr = smem_u32(q_s), do_addr = smem_u32(do_s), ring_addr = smem_u32(ring);
+    // S_r = Q K_r^T and dP_r = dO V_r^T for half r of the key tile in ring slot `slot`
+    auto issue_s = [&](int r, uint32_t slot) {
+      const uint32_t k_addr = opaque(ring_addr) + slot * C::kSlotBytes + r * kHalfBytes;
+      const uint64_t qd = sdesc_sw128(q_addr, 16, 1024), dod = sdesc_sw128(do_addr, 16, 1024);
+      const uint64_t kd = sdesc_sw128(k_addr, 16, 1024), vd = sdesc_sw128(k_addr + C::kTileBytes, 16, 1024);
+      if constexpr (D == 128) {
+        mma_bf16_ss_k8(tmem + 128 * r, qd, kd, idesc_s);
+        mma_bf16_ss_k8(tmem + 128 * r + BH2, dod, vd, idesc_s, smem_u32(&st_full[r]));
+      } else {
+        mma_bf16_ss_k4(tmem + 128 * r, qd, kd, idesc_s);
+        mma_bf16_ss_k4(tmem + 128 * r + BH2, dod, vd, idesc_s, smem_u32(&st_full[r]));
+      }
+    };
+    // dQ += dS_r K_r: A (dS_r) from TMEM, B (K_r) MN-major over the half's 64 keys
+    auto issue_acc = [&](int r, uint32_t slot, uint32_t acc, uint32_t bar0, uint32_t bar1) {
+      const uint32_t k_addr = opaque(ring_addr) + slot * C::kSlotBytes + r * kHalfBytes;
+      const uint64_t kb = sdesc_sw128(k_addr, C::kColBlockBytes, 1024);
+      mma_bf16_ts_k4(tmem + 2 * BT, tmem + 128 * r, kb, idesc_acc, acc, bar0, bar1);
+    };
+    uint32_t it = 0, g = 0, n_ne = 0;
     bool ok = true;
     for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
       const int n = key_tiles(p, p.n_qt - 1 - x / p.BH);
       if (n <= 0) continue;
       ok = warp_wait(&qd_full, n_ne & 1, abort_v, kTimeoutNs);
+      if (ok) ok = warp_wait(&full[it % kRing], (it / kRing) & 1, abort_v, kTimeoutNs);
       if (!ok) break;
-      for (int j = 0; j < n; ++j, ++it, ++gs) {
-        const uint32_t slot = it % kRing;
-        const uint32_t k_addr = opaque(ring_addr) + slot * C::kSlotBytes, v_addr = k_addr + C::kTileBytes;
-        ok = warp_wait(&full[slot], (it / kRing) & 1, abort_v, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
-        // S = Q K^T and dP = dO V^T (rows in the TMEM lanes), K steps over D
-        const uint64_t kd = sdesc_sw128(k_addr, 16, 1024), vd = sdesc_sw128(v_addr, 16, 1024);
-        if constexpr (D == 128) {
-          mma_bf16_ss_k8(tmem, qd, kd, idesc_s);
-          mma_bf16_ss_k8(tmem + BT, dod, vd, idesc_s, smem_u32(&s_full));
-        } else {
-          mma_bf16_ss_k4(tmem, qd, kd, idesc_s);
-          mma_bf16_ss_k4(tmem + BT, dod, vd, idesc_s, smem_u32(&s_full));
-        }
-        ok = warp_wait(&ds_full, gs & 1, abort_v, kTimeoutNs);
+      tc_fence_after();
+      issue_s(0, it % kRing);
+      issue_s(1, it % kRing);
+      for (int j = 0; j < n; ++j, ++it, ++g) {
+        const uint32_t slot = it % kRing, next = (it + 1) % kRing;
+        const bool more = j + 1 < n;
+        ok = warp_wait(&ds_full[0], g & 1, abort_v, kTimeoutNs);
         if (ok && j == 0 && n_ne > 0) ok = warp_wait(&acc_empty, (n_ne - 1) & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        // dQ += dS K: A (dS) from TMEM, B (K) MN-major over the keys
-        const uint64_t kb = sdesc_sw128(k_addr, C::kColBlockBytes, 1024);
-        mma_bf16_ts_k8(tmem + 2 * BT, tmem, kb, idesc_acc, j > 0 ? 1u : 0u, smem_u32(&empty[slot]),
-                       j + 1 == n ? smem_u32(&acc_full) : kNoBar);
+        issue_acc(0, slot, j > 0 ? 1u : 0u, kNoBar, kNoBar);
+        if (more) {
+          ok = warp_wait(&full[next], ((it + 1) / kRing) & 1, abort_v, kTimeoutNs);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(0, next);
+        }
+        ok = warp_wait(&ds_full[1], g & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        issue_acc(1, slot, 1u, smem_u32(&empty[slot]), more ? kNoBar : smem_u32(&acc_full));
+        if (more) issue_s(1, next);
       }
       if (!ok) break;
       mma_commit_elect(&qd_empty);  // Q and dO of this item are no longer read
@@ -536,22 +578,23 @@ __global__ void __maxnreg__(200)
     if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
     mma_commit_elect(&drain);
     warp_wait(&drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
+   }
   } else {
-    // ------------------------------------------------------------ compute (two threads per query row)
-    // Warp w serves the rows of TMEM lane quarter w % 4 and keys 64 * (w / 4) .. + 63 of
-    // each tile; its dS lands in columns 32 * (w / 4) .. + 31 (read first by the partner).
-    const int quarter = warp % 4, half = warp / 4;
+    // ------------------------------------------------------------ compute (one thread per query row)
+    // Warpgroup r takes half r (keys 64 r .. 64 r + 63) of every key tile; at the end of an
+    // item it writes columns r * D/2 .. of the row's dQ.
+    regs_increase<kRegsCompute>();
+    const int r = warp / 4, quarter = warp % 4;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t s_t = tmem + lane_off, dp_t = tmem + lane_off + BT, dq_t = tmem + lane_off + 2 * BT;
-    uint32_t gs = 0, n_ne = 0;
+    const uint32_t s_t = tmem + lane_off + 128 * r, dp_t = s_t + BH2, dq_t = tmem + lane_off + 2 * BT;
+    uint32_t g = 0, n_ne = 0;
     bool ok = true;
     for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
       const int i = p.n_qt - 1 - x / p.BH, bh = x % p.BH;
       const int n = key_tiles(p, i);
       const int row = i * BT + quarter * 32 + lane;
       const bool live = row < p.Sq;
-      // half h writes columns h * D/2 .. of this row's dQ
-      __nv_bfloat16* dqrow = p.dq + (static_cast<int64_t>(bh) * p.Sq + row) * D + half * (D / 2);
+      __nv_bfloat16* dqrow = p.dq + (static_cast<int64_t>(bh) * p.Sq + row) * D + r * (D / 2);
       if (n <= 0) {  // no key is visible to any row of this tile: zero gradient
         if (live) {
           uint4* a4 = reinterpret_cast<uint4*>(dqrow);
@@ -563,14 +606,13 @@ __global__ void __maxnreg__(200)
       const float lse2 = p.lse2[static_cast<int64_t>(bh) * p.Sq_pad + row];
       const float delt = p.delta[static_cast<int64_t>(bh) * p.Sq_pad + row];
       const int lim = p.causal ? min(p.Sk - 1, row + p.diag) : p.Sk - 1;  // last visible key
-      for (int j = 0; j < n; ++j, ++gs) {
-        ok = warp_wait(&s_full, gs & 1, abort_v, kTimeoutNs);
+      for (int j = 0; j < n; ++j, ++g) {
+        ok = warp_wait(&st_full[r], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
         uint32_t sv[64], dpv[64];
-        tmem_ld2x64_wait(s_t + 64 * half, dp_t + 64 * half, sv, dpv);
-        named_barrier_sync(1 + quarter, 64);  // both halves hold their S and dP columns
-        const int kmax = lim - j * BT - 64 * half;  // this thread's keys past kmax are masked
+        tmem_ld2x64_wait(s_t, dp_t, sv, dpv);
+        const int kmax = lim - j * BT - BH2 * r;  // this half's keys past kmax are masked
         uint32_t dsk[32];
 #pragma unroll
         for (int e2 = 0; e2 < 32; ++e2) {
@@ -583,10 +625,10 @@ __global__ void __maxnreg__(200)
           }
           dsk[e2] = pack_bf16x2(dd[0], dd[1]);
         }
-        tmem_st32(s_t + 32 * half, dsk);
+        tmem_st32(s_t, dsk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&ds_full);
+        mbar_arrive(&ds_full[r]);
       }
       if (!ok) break;
       ok = warp_wait(&acc_full, n_ne & 1, abort_v, kTimeoutNs);
@@ -596,7 +638,7 @@ __global__ void __maxnreg__(200)
 #pragma unroll
       for (int cb = 0; cb < D / 64; ++cb) {
         uint32_t a[32];
-        tmem_ld32_wait(dq_t + half * (D / 2) + 32 * cb, a);
+        tmem_ld32_wait(dq_t + r * (D / 2) + 32 * cb, a);
         if (live) {
           uint4* d4 = reinterpret_cast<uint4*>(dqrow + 32 * cb);
 #pragma unroll

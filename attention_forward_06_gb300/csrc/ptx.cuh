@@ -411,6 +411,18 @@ __device__ __forceinline__ void mma_bf16_ts_k8(uint32_t d_tmem, uint32_t a_tmem,
       ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(bar0), "r"(bar1)
       : "memory");
 }
+// TS form over 4 K steps of 16 (K = 64): A advances 8 TMEM columns, B 16 rows per step.
+__device__ __forceinline__ void mma_bf16_ts_k4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate, uint32_t bar0 = kNoBar, uint32_t bar1 = kNoBar) {
+  asm volatile(
+      "{\n\t.reg .pred e, t, f, c;\n\t.reg .b64 b;\n\t.reg .b32 ta;\n\t"
+      "setp.eq.b32 t, 1, 1;\n\tsetp.ne.b32 f, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, f;\n\t"
+      ATTN_MMA_TS_STEP(8, 128) ATTN_MMA_TS_STEP(16, 256) ATTN_MMA_TS_STEP(24, 384) ATTN_COMMITS(5, 6) "}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(bar0), "r"(bar1)
+      : "memory");
+}
 #undef ATTN_MMA_TS_STEP
 #undef ATTN_COMMITS
 
