@@ -68,8 +68,8 @@ struct BParams {
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  const float* lse2;   // [B*Hq][Sq_pad]: LSE * log2(e), +inf where P must be 0
-  const float* delta;  // [B*Hq][Sq_pad]: dO . O
+  const float* nlse2;   // [B*Hq][Sq_pad]: -LSE * log2(e), -inf where P must be 0
+  const float* ndelta;  // [B*Hq][Sq_pad]: -dO . O
   int Hq, Hkv, G, Sq, Sk, Sq_pad;
   int causal, diag;  // key j visible to row i iff !causal or j <= i + diag
   int n_qt, n_kt;    // 128-row query tiles, 128-key tiles
@@ -98,38 +98,45 @@ __device__ __forceinline__ void record_abort(volatile uint32_t* abort_flag, int 
 }
 
 // ---------------------------------------------------------------------------- prep
-// One warp per (row of B*Hq*Sq_pad): D_i = sum_d dO[i,d] O[i,d] (fp32, from the bf16 tensors)
-// and LSE_i * log2(e); rows past Sq and rows without keys (LSE = -inf) get +inf.
+// Rows of B*Hq*Sq_pad, 32 / (D/8) per warp, each lane reading 16 bytes of O and of dO:
+// -D_i = -sum_d dO[i,d] O[i,d] (fp32, from the bf16 tensors) and -LSE_i * log2(e); rows
+// past Sq and rows without keys (LSE = -inf) get -inf, so their P is 0.  The values are
+// stored negated so the kernels add them with packed FMAs.
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                             const __nv_bfloat16* __restrict__ dout,
-                                                            const float* __restrict__ lse, float* __restrict__ lse2,
-                                                            float* __restrict__ delta, int64_t BH, int Sq,
+                                                            const float* __restrict__ lse, float* __restrict__ nlse2,
+                                                            float* __restrict__ ndelta, int64_t BH, int Sq,
                                                             int Sq_pad) {
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  if (row >= BH * Sq_pad) return;
-  const int64_t bh = row / Sq_pad;
-  const int i = static_cast<int>(row % Sq_pad);
-  float acc = 0.0f, l2 = INFINITY;
-  if (i < Sq) {
-    const int64_t r = bh * Sq + i;
-    const uint32_t* o2 = reinterpret_cast<const uint32_t*>(o + r * D);
-    const uint32_t* g2 = reinterpret_cast<const uint32_t*>(dout + r * D);
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  const int lane = threadIdx.x % 32, sub = lane % kLanesPerRow;
+  const int64_t row =
+      (static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32) * kRowsPerWarp + lane / kLanesPerRow;
+  const bool in = row < BH * Sq_pad;
+  float acc = 0.0f, nl2 = -INFINITY;
+  if (in) {
+    const int64_t bh = row / Sq_pad;
+    const int i = static_cast<int>(row % Sq_pad);
+    if (i < Sq) {
+      const int64_t r = bh * Sq + i;
+      const uint4 a = reinterpret_cast<const uint4*>(o + r * D)[sub];
+      const uint4 b = reinterpret_cast<const uint4*>(dout + r * D)[sub];
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int e = lane; e < D / 2; e += 32) {
-      const uint32_t a = o2[e], b = g2[e];
-      acc = fmaf(bf16lo_to_f32(a), bf16lo_to_f32(b), acc);
-      acc = fmaf(bf16hi_to_f32(a), bf16hi_to_f32(b), acc);
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(bf16lo_to_f32(av[e]), bf16lo_to_f32(bv[e]), acc);
+        acc = fmaf(bf16hi_to_f32(av[e]), bf16hi_to_f32(bv[e]), acc);
+      }
+      const float L = lse[r];
+      nl2 = (L == -INFINITY) ? -INFINITY : -L * 1.4426950408889634f;
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    const float L = lse[r];
-    l2 = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
   }
-  if (lane == 0) {
-    lse2[row] = l2;
-    delta[row] = acc;
+#pragma unroll
+  for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (in && sub == 0) {
+    nlse2[row] = nl2;
+    ndelta[row] = -acc;
   }
 }
 
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = align_1024(smem_raw);
   uint8_t* k_s = smem;
   uint8_t* v_s = smem + C::kTileBytes;
-  uint8_t* ring = smem + 2 * C::kTileBytes;  // slot: Q, dO, lse2[128], delta[128]
+  uint8_t* ring = smem + 2 * C::kTileBytes;  // slot: Q, dO, -lse2[128], -delta[128]
   __shared__ uint64_t kv_full, kv_empty, full[kRing], empty[kRing], st_full[2], pt_full[2], acc_full, acc_empty,
       drain;
   __shared__ uint32_t tmem_slot, abort_flag;
@@ -232,8 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d_elect(sl + C::kTileBytes + cb * C::kColBlockBytes, &tdo, &full[slot], cb * 64, i * BT, bh);
         }
         const int64_t voff = static_cast<int64_t>(bh) * p.Sq_pad + i * BT;
-        bulk_load_1d_elect(sl + 2 * C::kTileBytes, p.lse2 + voff, C::kVecBytes, &full[slot]);
-        bulk_load_1d_elect(sl + 2 * C::kTileBytes + C::kVecBytes, p.delta + voff, C::kVecBytes, &full[slot]);
+        bulk_load_1d_elect(sl + 2 * C::kTileBytes, p.nlse2 + voff, C::kVecBytes, &full[slot]);
+        bulk_load_1d_elect(sl + 2 * C::kTileBytes + C::kVecBytes, p.ndelta + voff, C::kVecBytes, &full[slot]);
       }
     }
     if (!ok) {
@@ -283,6 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       issue_s(0, it % kRing);
       issue_s(1, it % kRing);
+      // K and V are read only by the S-type products: the next item's K and V may load
+      // once the item's last ones have been issued and completed
+      if (T == 1) mma_commit_elect(&kv_empty);
       for (int s = 0; s < T; ++s, ++it, ++g) {
         const uint32_t slot = it % kRing, next = (it + 1) % kRing;
         const bool more = s + 1 < T;
@@ -303,9 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // half 1's products are the slot's last readers; the item's last one completes dV and dK
         issue_acc(1, slot, 1u, smem_u32(&empty[slot]), more ? kNoBar : smem_u32(&acc_full));
         if (more) issue_s(1, next);
+        if (s + 2 == T) mma_commit_elect(&kv_empty);  // that was the item's last S-type pair
       }
       if (!ok) break;
-      mma_commit_elect(&kv_empty);  // K and V of this item are no longer read
       ++n_ne;
     }
     if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
@@ -344,32 +354,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < G * nI; ++s, ++it, ++g) {
         const int i = i0 + s % nI;
         const uint8_t* sl = ring + (it % kRing) * C::kSlotBytes;
-        const float4* lse2v = reinterpret_cast<const float4*>(sl + 2 * C::kTileBytes) + (BH2 / 4) * r;
-        const float4* deltav = reinterpret_cast<const float4*>(sl + 2 * C::kTileBytes + C::kVecBytes) + (BH2 / 4) * r;
+        const float4* nl4 = reinterpret_cast<const float4*>(sl + 2 * C::kTileBytes) + (BH2 / 4) * r;
+        const float4* nd4 = reinterpret_cast<const float4*>(sl + 2 * C::kTileBytes + C::kVecBytes) + (BH2 / 4) * r;
         // the slot's vectors have landed (this warp observes their copy itself), then S^T_r and dP^T_r
         ok = warp_wait(&full[it % kRing], (it / kRing) & 1, abort_v, kTimeoutNs);
         if (ok) ok = warp_wait(&st_full[r], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        // elements to mask: keys past Sk, and keys above the diagonal of a straddling tile
-        const bool diag_tile = p.causal && (j * BT + BT - 1 > i * BT + p.diag);
-        const int first_ok = key - p.diag - i * BT - BH2 * r;  // this half's rows e >= first_ok see the key
         uint32_t sv[64], dpv[64];
         tmem_ld2x64_wait(st_t, dpt_t, sv, dpv);
+        // masked elements (keys past Sk, keys above the diagonal of a straddling tile) get
+        // S = -inf, hence P = 0 (c > 0)
+        const bool diag_tile = p.causal && (j * BT + BT - 1 > i * BT + p.diag);
+        if (__any_sync(0xffffffffu, diag_tile || !key_live)) {
+          const int first_ok = key_live ? (diag_tile ? key - p.diag - i * BT - BH2 * r : 0) : BH2;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) sv[e] = e >= first_ok ? sv[e] : __float_as_uint(-INFINITY);
+        }
+        // P = exp2(S c - LSE log2 e) and dS = P (dP - D), two rows per packed operation
+        const uint64_t c2 = f2_pack(p.c, p.c);
         uint32_t pk[32], dsk[32];
 #pragma unroll
         for (int r4 = 0; r4 < 16; ++r4) {
-          const float4 l4 = lse2v[r4], d4 = deltav[r4];
+          const float4 l4 = nl4[r4], d4 = nd4[r4];
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dl[4] = {d4.x, d4.y, d4.z, d4.w};
           float pp[4], dd[4];
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             const int e = 4 * r4 + h;
-            const bool vis = key_live && (!diag_tile || e >= first_ok);
-            const float pr = vis ? ex2_approx(fmaf(__uint_as_float(sv[e]), p.c, -lv[h])) : 0.0f;
-            pp[h] = pr;
-            dd[h] = pr * (__uint_as_float(dpv[e]) - dl[h]);
+            pp[h] = ex2_approx(fmaf(__uint_as_float(sv[e]), p.c, lv[h]));
           }
+          float y0, y1, y2, y3;
+          f2_unpack(fmul2(f2_pack(pp[0], pp[1]), fadd2(f2_pack(__uint_as_float(dpv[4 * r4]), __uint_as_float(dpv[4 * r4 + 1])), f2_pack(dl[0], dl[1]))), y0, y1);
+          f2_unpack(fmul2(f2_pack(pp[2], pp[3]), fadd2(f2_pack(__uint_as_float(dpv[4 * r4 + 2]), __uint_as_float(dpv[4 * r4 + 3])), f2_pack(dl[2], dl[3]))), y2, y3);
+          dd[0] = y0; dd[1] = y1; dd[2] = y2; dd[3] = y3;
           pk[2 * r4] = pack_bf16x2(pp[0], pp[1]);
           pk[2 * r4 + 1] = pack_bf16x2(pp[2], pp[3]);
           dsk[2 * r4] = pack_bf16x2(dd[0], dd[1]);
@@ -551,6 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       issue_s(0, it % kRing);
       issue_s(1, it % kRing);
+      // Q and dO are read only by the S-type products (see the dK/dV kernel)
+      if (n == 1) mma_commit_elect(&qd_empty);
       for (int j = 0; j < n; ++j, ++it, ++g) {
         const uint32_t slot = it % kRing, next = (it + 1) % kRing;
         const bool more = j + 1 < n;
@@ -570,9 +590,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_acc(1, slot, 1u, smem_u32(&empty[slot]), more ? kNoBar : smem_u32(&acc_full));
         if (more) issue_s(1, next);
+        if (j + 2 == n) mma_commit_elect(&qd_empty);  // that was the item's last S-type pair
       }
       if (!ok) break;
-      mma_commit_elect(&qd_empty);  // Q and dO of this item are no longer read
       ++n_ne;
     }
     if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
@@ -603,8 +623,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const float lse2 = p.lse2[static_cast<int64_t>(bh) * p.Sq_pad + row];
-      const float delt = p.delta[static_cast<int64_t>(bh) * p.Sq_pad + row];
+      const float nl = p.nlse2[static_cast<int64_t>(bh) * p.Sq_pad + row];
+      const float nd = p.ndelta[static_cast<int64_t>(bh) * p.Sq_pad + row];
+      const uint64_t c2 = f2_pack(p.c, p.c), nl2 = f2_pack(nl, nl), nd2 = f2_pack(nd, nd);
       const int lim = p.causal ? min(p.Sk - 1, row + p.diag) : p.Sk - 1;  // last visible key
       for (int j = 0; j < n; ++j, ++g) {
         ok = warp_wait(&st_full[r], g & 1, abort_v, kTimeoutNs);
@@ -612,18 +633,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint32_t sv[64], dpv[64];
         tmem_ld2x64_wait(s_t, dp_t, sv, dpv);
-        const int kmax = lim - j * BT - BH2 * r;  // this half's keys past kmax are masked
+        // keys past kmax (above the diagonal, or past Sk) get S = -inf, hence P = 0 (c > 0)
+        const int kmax = lim - j * BT - BH2 * r;
+        if (__any_sync(0xffffffffu, kmax < BH2 - 1)) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) sv[e] = e <= kmax ? sv[e] : __float_as_uint(-INFINITY);
+        }
+        // dS = P (dP - D) with P = exp2(S c - LSE log2 e), two keys per packed operation
         uint32_t dsk[32];
 #pragma unroll
         for (int e2 = 0; e2 < 32; ++e2) {
-          float dd[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = 2 * e2 + h;
-            const float pr = e <= kmax ? ex2_approx(fmaf(__uint_as_float(sv[e]), p.c, -lse2)) : 0.0f;
-            dd[h] = pr * (__uint_as_float(dpv[e]) - delt);
-          }
-          dsk[e2] = pack_bf16x2(dd[0], dd[1]);
+          float x0, x1, y0, y1;
+          f2_unpack(ffma2(f2_pack(__uint_as_float(sv[2 * e2]), __uint_as_float(sv[2 * e2 + 1])), c2, nl2), x0, x1);
+          const uint64_t pp = f2_pack(ex2_approx(x0), ex2_approx(x1));
+          const uint64_t dp = fadd2(f2_pack(__uint_as_float(dpv[2 * e2]), __uint_as_float(dpv[2 * e2 + 1])), nd2);
+          f2_unpack(fmul2(pp, dp), y0, y1);
+          dsk[e2] = pack_bf16x2(y0, y1);
         }
         tmem_st32(s_t, dsk);
         tmem_wait_st();
@@ -724,7 +749,8 @@ int launch_all(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
                BParams prm, const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* lse, float* lse2,
                float* delta, int sms, cudaStream_t stream) {
   const int64_t prep_rows = static_cast<int64_t>(prm.BH) * prm.Sq_pad;
-  attn_bwd_prep_kernel<D><<<static_cast<unsigned>((prep_rows + 7) / 8), 256, 0, stream>>>(
+  const int64_t prep_warps = (prep_rows + 32 / (D / 8) - 1) / (32 / (D / 8));
+  attn_bwd_prep_kernel<D><<<static_cast<unsigned>((prep_warps + 7) / 8), 256, 0, stream>>>(
       o, dout, lse, lse2, delta, prm.BH, prm.Sq, prm.Sq_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
@@ -758,7 +784,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   // ---- argument checks (host only, before any CUDA call)
   if (B < 0 || Sq < 0 || Sk < 0 || Hq < 1 || Hkv < 1) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0 || causal < 0 || causal > 2 || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || causal < 0 || causal > 2 || !(std::isfinite(scale) && scale > 0.0f)) return ATTN_ERR_INVALID_ARG;
   if (static_cast<int64_t>(B) * Hq > INT32_MAX / 2 || padded_rows(Sq) > INT32_MAX / 2) return ATTN_ERR_INVALID_ARG;
   if (B == 0) return ATTN_OK;
   const size_t qb = static_cast<size_t>(B) * Hq * Sq * D * 2, kb = static_cast<size_t>(B) * Hkv * Sk * D * 2;
@@ -810,10 +836,10 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   prm.dk = static_cast<__nv_bfloat16*>(dk);
   prm.dv = static_cast<__nv_bfloat16*>(dv);
   const size_t one = wb / 2;
-  float* lse2 = static_cast<float*>(workspace);
+  float* lse2 = static_cast<float*>(workspace);  // stored negated, as the kernels use them
   float* delta = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + one);
-  prm.lse2 = lse2;
-  prm.delta = delta;
+  prm.nlse2 = lse2;
+  prm.ndelta = delta;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
   prm.G = Hq / Hkv;

@@ -992,7 +992,7 @@ int prepare_launch(const void* q, const void* k, const void* v, void* o, float* 
   if (D != 64 && D != 128) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (causal < 0 || causal > 2) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.0f)) return ATTN_ERR_INVALID_ARG;  // masking relies on scale > 0
   if (n_splits < 1 || n_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
   const int64_t q_elems = static_cast<int64_t>(B) * Hq * Sq * D;
   const int64_t kv_elems = static_cast<int64_t>(B) * Hkv * Sk * D;

@@ -18,8 +18,8 @@
  * Layout (contiguous, row-major, device memory, 16-byte aligned):
  *     q, o, dout, dq [B][Hq][Sq][D] bf16    k, v, dk, dv [B][Hkv][Sk][D] bf16
  *     lse [B][Hq][Sq] fp32 (the forward's)  workspace: attn_bwd_workspace_size bytes
- * D is 64 or 128; Hq a multiple of Hkv; causal as in attn_fwd (0, 1 bottom-right,
- * 2 top-left).  Rows without keys get dq = 0; keys no row sees get dk = dv = 0.
+ * D is 64 or 128; Hq a multiple of Hkv; scale finite and positive (the
+ * forward's); causal as in attn_fwd (0, 1 bottom-right, 2 top-left).  Rows without keys get dq = 0; keys no row sees get dk = dv = 0.
  *
  * Precision.  bf16 inputs; S, dP and the three gradients accumulate in fp32 on
  * the tensor cores; P and dS are rounded to bf16 before the products that use

@@ -26,8 +26,9 @@
  * Layout (all contiguous, row-major, device memory):
  *     q [B][Hq][Sq][D] bf16     k, v [B][Hkv][Sk][D] bf16
  *     o [B][Hq][Sq][D] bf16     lse  [B][Hq][Sq] fp32
- * D must be 64 or 128; Hq must be a multiple of Hkv; every pointer must be
- * 16-byte aligned.  o and lse must not overlap q, k, v or each other.
+ * D must be 64 or 128; Hq must be a multiple of Hkv; scale must be finite and
+ * positive (1/sqrt(D) is the usual value); every pointer must be 16-byte
+ * aligned.  o and lse must not overlap q, k, v or each other.
  *
  * Ownership and execution.  The caller owns every buffer.  attn_fwd allocates
  * no device memory; it enqueues one kernel on `stream` (0 = legacy default
@@ -55,7 +56,8 @@ extern "C" {
 /* Status codes (0 = success). */
 #define ATTN_OK 0
 #define ATTN_ERR_INVALID_ARG 1        /* a size < 0, Hq or Hkv < 1, D not 64/128, Hq % Hkv, causal not 0..2,
-                                         overlapping outputs, or a size beyond the 32-bit index range */
+                                         scale not finite and > 0, overlapping outputs, or a size beyond
+                                         the 32-bit index range */
 #define ATTN_ERR_NULL_PTR 2           /* a required pointer is NULL */
 #define ATTN_ERR_MISALIGNED 3         /* a pointer is not 16-byte aligned */
 #define ATTN_ERR_UNSUPPORTED_DEVICE 4 /* the current device is not compute capability 10.3 (sm_103a) */

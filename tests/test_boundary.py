@@ -69,6 +69,7 @@ def call(q=Q, k=K, v=V, o=O, lse=L, **kw):
 @pytest.mark.parametrize("kw", [
     dict(D=96), dict(D=0), dict(D=256), dict(Hq=3, Hkv=2), dict(Hkv=0), dict(Hq=0), dict(causal=3),
     dict(causal=-1), dict(B=-1), dict(Sq=-5), dict(Sk=-1), dict(scale=float("nan")), dict(scale=float("inf")),
+    dict(scale=0.0), dict(scale=-0.1),  # the masking takes scale > 0
 ])
 def test_invalid_arguments(kw):
     assert call(**kw) == ops.ATTN_ERR_INVALID_ARG
@@ -176,8 +177,10 @@ def test_bwd_workspace_formula_and_invalid_arguments():
     call = lambda **kw: lib.attn_bwd(*[kw.get(n, a) for n, a in zip(
         ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv"),
         (0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000, 0x800000, 0x880000))],
-        1, 4, kw.get("Hkv", 2), 64, 64, kw.get("D", 128), 1, 0.1, kw.get("ws", W), 1 << 20, None)
+        1, 4, kw.get("Hkv", 2), 64, 64, kw.get("D", 128), 1, kw.get("scale", 0.1), kw.get("ws", W), 1 << 20, None)
     assert call(D=96) == ops.ATTN_ERR_INVALID_ARG
+    assert call(scale=0.0) == ops.ATTN_ERR_INVALID_ARG
+    assert call(scale=-0.5) == ops.ATTN_ERR_INVALID_ARG
     assert call(Hkv=3) == ops.ATTN_ERR_INVALID_ARG
     assert call(dq=0) == ops.ATTN_ERR_NULL_PTR
     assert call(ws=0) == ops.ATTN_ERR_NULL_PTR
