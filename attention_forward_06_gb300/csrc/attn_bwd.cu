@@ -140,6 +140,14 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16*
   }
 }
 
+// The k-th work item of this CTA.  Items are listed heaviest first and dealt in
+// rounds of gridDim.x, forwards on even rounds and backwards on odd ones, so every
+// CTA gets a similar amount of work (every role walks the same sequence).
+__device__ __forceinline__ int item_of(int k) {
+  const int c = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
+  return k * G + ((k & 1) ? G - 1 - c : c);
+}
+
 // Query tiles [i0, n_qt) that see key tile j (none when i0 >= n_qt).
 __device__ __forceinline__ int first_qtile(const BParams& p, int j) {
   if (!p.causal) return 0;
@@ -210,7 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     uint32_t it = 0, n_ne = 0;  // ring loads issued; items with query tiles
     bool ok = true;
-    for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
+    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
+      const int x = item_of(k);
+      if (x >= p.n_items) continue;
       const int j = x / nz, z = x % nz;
       const int i0 = first_qtile(p, j);
       const int nI = p.n_qt - i0;
@@ -279,7 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     uint32_t it = 0, g = 0, n_ne = 0;  // ring uses, steps (st/pt phases), items with query tiles
     bool ok = true;
-    for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
+    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
+      const int x = item_of(k);
+      if (x >= p.n_items) continue;
       const int j = x / nz;
       const int nI = p.n_qt - first_qtile(p, j);
       if (nI <= 0) continue;
@@ -336,16 +348,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kk = quarter * 32 + lane;
     uint32_t it = 0, g = 0, n_ne = 0;
     bool ok = true;
-    for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
-      const int j = x / nz, z = x % nz;
+    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
+      const int x = item_of(k);
+      if (x >= p.n_items) continue;
+      const int j = x / nz;
       const int i0 = first_qtile(p, j);
       const int nI = p.n_qt - i0;
       const int key = j * BT + kk;
       const bool key_live = key < p.Sk;
-      __nv_bfloat16* grow = (r == 0 ? p.dv : p.dk) + (static_cast<int64_t>(z) * p.Sk + key) * D;
+      // this key's dV (warpgroup 0) or dK (warpgroup 1) row
+      auto grad_row = [&]() { return (r == 0 ? p.dv : p.dk) + (static_cast<int64_t>(x % nz) * p.Sk + key) * D; };
       if (nI <= 0) {  // no query row sees this key tile: zero gradients
         if (key_live) {
-          uint4* a4 = reinterpret_cast<uint4*>(grow);
+          uint4* a4 = reinterpret_cast<uint4*>(grad_row());
 #pragma unroll
           for (int v4 = 0; v4 < D / 8; ++v4) a4[v4] = make_uint4(0u, 0u, 0u, 0u);
         }
@@ -407,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n_ne;
       tc_fence_after();
       const float mul = r == 0 ? 1.0f : p.scale;
+      __nv_bfloat16* grow = grad_row();
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
         uint32_t a[32];
@@ -501,7 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     uint32_t it = 0, n_ne = 0;
     bool ok = true;
-    for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
+    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
+      const int x = item_of(k);
+      if (x >= p.n_items) continue;
       const int i = p.n_qt - 1 - x / p.BH, bh = x % p.BH;
       const int n = key_tiles(p, i);
       if (n <= 0) continue;
@@ -560,7 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     uint32_t it = 0, g = 0, n_ne = 0;
     bool ok = true;
-    for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
+    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
+      const int x = item_of(k);
+      if (x >= p.n_items) continue;
       const int n = key_tiles(p, p.n_qt - 1 - x / p.BH);
       if (n <= 0) continue;
       ok = warp_wait(&qd_full, n_ne & 1, abort_v, kTimeoutNs);
@@ -609,7 +629,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_t = tmem + lane_off + 128 * r, dp_t = s_t + BH2, dq_t = tmem + lane_off + 2 * BT;
     uint32_t g = 0, n_ne = 0;
     bool ok = true;
-    for (int x = blockIdx.x; x < p.n_items && ok; x += gridDim.x) {
+    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
+      const int x = item_of(k);
+      if (x >= p.n_items) continue;
       const int i = p.n_qt - 1 - x / p.BH, bh = x % p.BH;
       const int n = key_tiles(p, i);
       const int row = i * BT + quarter * 32 + lane;
