@@ -9,8 +9,8 @@
 //     dS_ij = P_ij (dP_ij - D_i),   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i.
 //
 // Three kernels on the caller's stream:
-//   attn_bwd_prep_kernel   D_i = dO_i . O_i and LSE_i * log2(e) into the workspace
-//                          (+inf for rows without keys and for padding rows, so their P is 0)
+//   attn_bwd_prep_kernel   -D_i = -dO_i . O_i and -LSE_i * log2(e) into the workspace
+//                          (-inf for rows without keys and for padding rows, so their P is 0)
 //   attn_bwd_dkdv_kernel   one (batch, kv head, 128-key tile) per work item: streams the
 //                          query tiles of every query head of the group, with the keys in
 //                          the TMEM lanes: S^T = K Q^T and dP^T = V dO^T (SS form), P^T and
@@ -18,9 +18,11 @@
 //                          form, A from TMEM) accumulate in TMEM across the whole item
 //   attn_bwd_dq_kernel     one (batch, query head, 128-row tile) per item: S = Q K^T,
 //                          dP = dO V^T, dS into TMEM, dQ += dS K
-// Each kernel: warps 0-7 compute (two threads per TMEM lane, each on half of the
-// tile's columns), warp 8 loads with TMA, warp 9 issues the tcgen05 MMAs; every wait
-// is bounded as in the forward.
+// Each kernel takes a step (a 128-row query tile, or a 128-key tile) in two 64-wide
+// halves held in two TMEM regions; warpgroup r (warps 4r .. 4r+3, one thread per TMEM
+// lane) computes half r while the tensor cores run the other half's products.  Warp 8
+// loads with TMA, warp 9 issues the tcgen05 MMAs, warps 10-11 idle; every wait is
+// bounded as in the forward.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

@@ -122,7 +122,7 @@ struct Params {
   int n_splits;
   float* o_part;    // [n_splits][BH][Sq][D]
   float* lse_part;  // [n_splits][BH][Sq]
-  int sched_slot;   // counter pair of the dynamic schedule used by this launch
+  int sched_slot;   // which schedule counter this launch claims items from
   // block-sparse mode: bit-packed mask [B][mask_heads][n_qtiles][mask_words], one bit per
   // (128-row query block, 128-key block), bit kb % 32 of word kb / 32
   const uint32_t* mask;
@@ -879,7 +879,7 @@ int cuda_fail(cudaError_t e) {
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<unsigned int> g_launch_seq{0};  // picks each launch's schedule counter pair
+std::atomic<unsigned int> g_launch_seq{0};  // picks each launch's schedule counter
 std::mutex g_dev_mutex;
 int g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 unsupported
 int g_dev_sms[kMaxDevices];    // streaming multiprocessors per device
