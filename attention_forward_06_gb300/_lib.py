@@ -30,6 +30,8 @@ SIGNATURES = {
         "attn_fwd_splitkv_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _c_int, _vp]),
         "attn_fwd_blocksparse": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp, _c_int, _vp]),
         "attn_fwd_block_mask_words": (ctypes.c_size_t, [_c_int] * 4),
+        "attn_fwd_ordered": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp, _c_int, _vp]),
+        "attn_fwd_tile_order_entries": (ctypes.c_size_t, [_c_int] * 4),
     },
     "attn_bwd": {
         "attn_bwd": (_c_int, [_vp] * 9 + [_c_int] * 7 + [_c_float, _vp, ctypes.c_size_t, _vp]),

@@ -129,6 +129,11 @@ struct Params {
   int mask_heads;  // 1 (one mask for every head) or Hq
   int mask_words;  // words per mask row: ceil(ceil(Sk / 128) / 32)
   int n_qtiles;    // ceil(Sq / 128)
+  // ordered mode: key-tile order [B][order_heads][n_qblocks][order_len], one row per
+  // 256-row query block (the item), visited in row order
+  const int32_t* order;
+  int order_heads;  // 1 (one order for every head) or Hq
+  int order_len;    // entries per row: ceil(Sk / 128)
 };
 
 struct Item {
@@ -215,6 +220,61 @@ __device__ __forceinline__ int sparse_tiles(const Params& p, const Item& it) {
   return n;
 }
 
+// Ordered mode (the priority-ordered visitation of page "CoSA: Accelerating Long-Context
+// Inference via Proxy-Kernel Co-Designed Sparse Attention": the kernel reads the key
+// tiles in the order a priority list gives).  An item visits, in row order, every
+// entry e of its row with 0 <= e < its causal key-tile bound.  The row is scanned 32
+// entries at a time: each lane holds one entry of the current window and a ballot
+// marks the entries visited, so a warp finds the next tile with find-first-set and a
+// shuffle instead of a chain of dependent loads.
+__device__ __forceinline__ const int32_t* order_row(const Params& p, const Item& it) {
+  const int b = it.bh / p.Hq;
+  const int ho = p.order_heads == 1 ? 0 : it.bh % p.Hq;
+  const int qb = it.q0 / ROWS_PER_ITEM;
+  return p.order + ((static_cast<int64_t>(b) * p.order_heads + ho) * p.n_qblocks + qb) * p.order_len;
+}
+
+// window w of an order row: this lane's entry in `val` (-1 past the row), and the
+// ballot of the entries visited under the key-tile bound n
+__device__ __forceinline__ uint32_t order_window(const int32_t* row, int len, int w, int n, int& val) {
+  const int e = 32 * w + static_cast<int>(threadIdx.x % 32);
+  val = e < len ? __ldg(row + e) : -1;
+  return __ballot_sync(0xffffffffu, val >= 0 && val < n);
+}
+
+// number of key tiles an item visits in ordered mode (the whole warp calls it)
+__device__ __forceinline__ int ordered_tiles(const Params& p, const Item& it) {
+  const int32_t* row = order_row(p, it);
+  int n = 0, v;
+  for (int w = 0; 32 * w < p.order_len; ++w) n += __popc(order_window(row, p.order_len, w, it.n_tiles, v));
+  return n;
+}
+
+// Walks the visited entries of an order row, one window at a time (warp-uniform).
+struct OrderWalk {
+  const int32_t* row = nullptr;
+  int len = 0, bound = 0, w = 0, val = -1;
+  uint32_t cur = 0;
+  __device__ __forceinline__ void start(const int32_t* r, int l, int n) {
+    row = r;
+    len = l;
+    bound = n;
+    w = 0;
+    cur = order_window(row, len, 0, bound, val);
+  }
+  // the next visited tile (0 if the row has no more, which the counts rule out
+  // unless the row changed under the call)
+  __device__ __forceinline__ int next() {
+    const int w_end = (len + 31) / 32;
+    while (cur == 0 && w + 1 < w_end) cur = order_window(row, len, ++w, bound, val);
+    const int bit = cur ? __ffs(cur) - 1 : 0;
+    const int tile = __shfl_sync(0xffffffffu, val, bit);
+    const bool found = cur != 0;
+    cur &= cur - 1;
+    return found ? tile : 0;
+  }
+};
+
 __device__ int g_status;  // sticky: 0 = fine, else the site of the first wait that ran out
 
 // Dynamic schedule.  CTA c starts on item c; later items are claimed in list
@@ -247,13 +307,17 @@ __device__ __forceinline__ void record_abort(volatile uint32_t* abort_flag, int 
   atomicCAS(&g_status, 0, site);
 }
 
-template <int D, bool SPLIT, bool SPARSE>
+template <int D, bool SPLIT, bool SPARSE, bool ORDERED = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
                     const Params p) {
   using C = Cfg<D>;
   constexpr int S = C::kStages;
+  // block-sparse and ordered modes: the producer counts each item's key tiles and
+  // publishes the count with the item; every role walks the same tile sequence
+  constexpr bool LISTED = SPARSE || ORDERED;
+  static_assert(!(SPARSE && ORDERED) && !(SPLIT && (SPARSE || ORDERED)), "one visiting mode at a time");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint8_t* q_s = smem;               // Q tile t at q_s + t * kTileBytes
@@ -265,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t stage_full[QTILES], stage_rel[QTILES], mma_drain;
   __shared__ uint64_t seq_full[kSeqSlots], seq_empty[kSeqSlots];
   __shared__ int item_seq[kSeqSlots];  // the CTA's k-th item at slot k % kSeqSlots (-1: no more)
-  __shared__ int item_ntiles[kSeqSlots];  // block-sparse mode: its marked key tiles (counted by the producer)
+  __shared__ int item_ntiles[kSeqSlots];  // block-sparse / ordered mode: its key tiles (counted by the producer)
   __shared__ uint32_t tmem_base_slot;
   __shared__ uint32_t abort_flag;
 
@@ -342,19 +406,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = warp_wait(&seq_empty[k % kSeqSlots], (k / kSeqSlots - 1) & 1, abort_v, kTimeoutNs);
         if (!ok) break;
       }
-      int n_marked = 0;  // block-sparse mode: the item's marked key tiles
+      int n_marked = 0;  // block-sparse / ordered mode: the key tiles the item visits
       if constexpr (SPARSE) {
         if (more) n_marked = sparse_tiles(p, item_at<SPLIT, SPARSE>(p, x));
+      } else if constexpr (ORDERED) {
+        if (more) n_marked = ordered_tiles(p, item_at<SPLIT>(p, x));
       }
       if (lane == 0) {
         item_seq[k % kSeqSlots] = more ? x : -1;
-        if constexpr (SPARSE) item_ntiles[k % kSeqSlots] = n_marked;
+        if constexpr (LISTED) item_ntiles[k % kSeqSlots] = n_marked;
         mbar_arrive(&seq_full[k % kSeqSlots]);
       }
       __syncwarp();
       if (!more) break;
       const Item it = item_at<SPLIT, SPARSE>(p, x);
-      const int n_tiles = SPARSE ? n_marked : it.n_tiles;
+      const int n_tiles = LISTED ? n_marked : it.n_tiles;
       // The next item is claimed once this item's loads are all issued (about two
       // key tiles before its end), so items are handed out in the order CTAs free up.
       auto claim = [&]() {
@@ -390,6 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mrows = mask_rows(p, it);
         mcur = union_word(mrows, 0, it.n_tiles);
       }
+      OrderWalk owalk;  // ordered mode: the item's row of the order
+      if constexpr (ORDERED) owalk.start(order_row(p, it), p.order_len, it.n_tiles);
       for (int i = 0; i < 2 * n_tiles; ++i) {  // K_j is load 2j, V_j is load 2j+1
         if (k == 0 && i == 2) {
           // all CTAs start at once: let the first item's Q and K_0 land before streaming
@@ -411,6 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             kb = mcur ? 32 * mw + __ffs(mcur) - 1 : 0;
             mcur &= mcur - 1;
           }
+        } else if constexpr (ORDERED) {
+          if (!(i & 1)) kb = owalk.next();  // the next tile of the order
         } else {
           kb = it.j0 + (i >> 1);
         }
@@ -478,9 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       int x, n_marked = 0;
-      ok = next_item(k, x, SPARSE ? &n_marked : nullptr);
+      ok = next_item(k, x, LISTED ? &n_marked : nullptr);
       if (!ok || x < 0) break;
-      const int n = SPARSE ? n_marked : item_at<SPLIT>(p, x).n_tiles;
+      const int n = LISTED ? n_marked : item_at<SPLIT>(p, x).n_tiles;
       if (n == 0) continue;
       ok = warp_wait(&q_full, n_done & 1, abort_v, kTimeoutNs);
       if (ok) ok = wait_kv(kv_it);
@@ -537,11 +607,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       int x, n_marked = 0;
-      ok = next_item(k, x, SPARSE ? &n_marked : nullptr);
+      ok = next_item(k, x, LISTED ? &n_marked : nullptr);
       if (!ok || x < 0) break;
       if constexpr (!SPLIT) {  // split-key partials are written by the softmax warps directly
         const Item it = item_at<SPLIT, SPARSE>(p, x);
-        if ((SPARSE ? n_marked : it.n_tiles) == 0) continue;
+        if ((LISTED ? n_marked : it.n_tiles) == 0) continue;
         for (int t = 0; t < QTILES && ok; ++t) {
           ok = warp_wait(&stage_full[t], e_seen[t] & 1, abort_v, kTimeoutNs);
           if (!ok) break;
@@ -575,14 +645,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int k = 0; ok; ++k) {
       int x, n_marked = 0;
-      ok = next_item(k, x, SPARSE ? &n_marked : nullptr);
+      ok = next_item(k, x, LISTED ? &n_marked : nullptr);
       if (!ok) {
         if (lane == 0) record_abort(abort_v, kSiteSoftmax);
         break;
       }
       if (x < 0) break;
       const Item it = item_at<SPLIT, SPARSE>(p, x);
-      const int n_tiles = SPARSE ? n_marked : it.n_tiles;  // key tiles the item visits
+      const int n_tiles = LISTED ? n_marked : it.n_tiles;  // key tiles the item visits
       const int row = it.q0 + t * BM + quarter * 32 + lane;  // global query row
       const bool live = row < p.Sq;
       __nv_bfloat16* orow = p.o + (static_cast<int64_t>(it.bh) * p.Sq + row) * D;
@@ -626,6 +696,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mcur = union_word(mrows, 0, it.n_tiles);
         mown = t == 0 ? __ldg(mrows.r0) : (mrows.r1 ? __ldg(mrows.r1) : 0u);
       }
+      OrderWalk owalk;  // ordered mode: the same walk as the producer's
+      if constexpr (ORDERED) owalk.start(order_row(p, it), p.order_len, it.n_tiles);
       for (int j = 0; j < n_tiles; ++j, ++g) {
         ok = warp_wait(&s_full[t], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
@@ -644,6 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           jg = 32 * mw + bit;
           own = (mown >> bit) & 1u;
           mcur &= mcur - 1;
+        } else if constexpr (ORDERED) {
+          jg = owalk.next();
         }
         // the tile is unmarked for this Q tile, or straddles the diagonal or the end of K
         const bool masked = !own || jg * BN + BN - 1 > lim_tile;
@@ -904,10 +978,12 @@ int prepare_device(int dev) {
   g_dev_sms[dev] = sms;
   const void* k128[] = {reinterpret_cast<const void*>(attn_fwd_kernel<128, false, false>),
                         reinterpret_cast<const void*>(attn_fwd_kernel<128, true, false>),
-                        reinterpret_cast<const void*>(attn_fwd_kernel<128, false, true>)};
+                        reinterpret_cast<const void*>(attn_fwd_kernel<128, false, true>),
+                        reinterpret_cast<const void*>(attn_fwd_kernel<128, false, false, true>)};
   const void* k64[] = {reinterpret_cast<const void*>(attn_fwd_kernel<64, false, false>),
                        reinterpret_cast<const void*>(attn_fwd_kernel<64, true, false>),
-                       reinterpret_cast<const void*>(attn_fwd_kernel<64, false, true>)};
+                       reinterpret_cast<const void*>(attn_fwd_kernel<64, false, true>),
+                       reinterpret_cast<const void*>(attn_fwd_kernel<64, false, false, true>)};
   for (const void* f : k128)
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<128>::kSmemBytes);
@@ -1052,6 +1128,9 @@ int prepare_launch(const void* q, const void* k, const void* v, void* o, float* 
   prm.lse_part = nullptr;
   prm.sched_slot = static_cast<int>(g_launch_seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
   prm.mask = nullptr;
+  prm.order = nullptr;
+  prm.order_heads = 1;
+  prm.order_len = 0;
   prm.mask_heads = 1;
   prm.mask_words = 0;
   prm.n_qtiles = static_cast<int>((Sq + BM - 1) / BM);
@@ -1060,10 +1139,10 @@ int prepare_launch(const void* q, const void* k, const void* v, void* o, float* 
   return ATTN_OK;
 }
 
-template <int D, bool SPLIT, bool SPARSE = false>
+template <int D, bool SPLIT, bool SPARSE = false, bool ORDERED = false>
 int launch(const Launch& L, cudaStream_t stream) {
-  attn_fwd_kernel<D, SPLIT, SPARSE><<<L.grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(L.tq, L.tk, L.tv, L.to,
-                                                                                     L.prm);
+  attn_fwd_kernel<D, SPLIT, SPARSE, ORDERED><<<L.grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(L.tq, L.tk, L.tv,
+                                                                                              L.to, L.prm);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -1196,6 +1275,37 @@ int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, f
   L.prm.mask_heads = mask_heads;
   L.prm.mask_words = static_cast<int>(((static_cast<int64_t>(Sk) + BN - 1) / BN + 31) / 32);
   return D == 128 ? launch<128, false, true>(L, stream) : launch<64, false, true>(L, stream);
+}
+
+size_t attn_fwd_tile_order_entries(int B, int order_heads, int Sq, int Sk) {
+  if (B < 0 || order_heads < 1 || Sq < 0 || Sk < 0) return 0;
+  const int64_t kblocks = (static_cast<int64_t>(Sk) + BN - 1) / BN;
+  const int64_t qblocks = (static_cast<int64_t>(Sq) + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM;
+  return static_cast<size_t>(B) * order_heads * qblocks * kblocks;
+}
+
+int attn_fwd_ordered(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+                     int Sk, int D, int causal, float scale, const int32_t* tile_order, int order_heads,
+                     cudaStream_t stream) {
+  // the order's own checks (host only, before any CUDA call), then the common ones
+  if (Hq < 1 || (order_heads != 1 && order_heads != Hq)) return ATTN_ERR_INVALID_ARG;
+  const size_t entries = (B > 0 && Sq > 0 && Sk > 0) ? attn_fwd_tile_order_entries(B, order_heads, Sq, Sk) : 0;
+  if (entries > 0) {
+    if (!tile_order) return ATTN_ERR_NULL_PTR;
+    if ((reinterpret_cast<uintptr_t>(tile_order) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+    if (D > 0) {
+      const size_t ob = entries * 4;
+      const size_t qb = static_cast<size_t>(B) * Hq * Sq * D * 2, lb = static_cast<size_t>(B) * Hq * Sq * 4;
+      if (overlaps(tile_order, ob, o, qb) || overlaps(tile_order, ob, lse, lb)) return ATTN_ERR_INVALID_ARG;
+    }
+  }
+  Launch L;
+  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, 1, &L);
+  if (st != ATTN_OK || L.empty) return st;
+  L.prm.order = tile_order;
+  L.prm.order_heads = order_heads;
+  L.prm.order_len = static_cast<int>((static_cast<int64_t>(Sk) + BN - 1) / BN);
+  return D == 128 ? launch<128, false, false, true>(L, stream) : launch<64, false, false, true>(L, stream);
 }
 
 int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,

@@ -197,6 +197,47 @@ def attn_fwd_blocksparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bloc
     return o, lse
 
 
+ORDER_ROWS = 256  # query rows sharing one key-tile order (ATTN_ORDER_ROWS)
+ORDER_KEYS = 128  # keys per key tile of an order (ATTN_ORDER_KEYS)
+
+
+def tile_order_entries(B: int, order_heads: int, Sq: int, Sk: int) -> int:
+    return int(load().attn_fwd_tile_order_entries(B, order_heads, Sq, Sk))
+
+
+def attn_fwd_ordered(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, tile_order: torch.Tensor,
+                     causal: int = 1, scale: float | None = None, o: torch.Tensor | None = None,
+                     lse: torch.Tensor | None = None, stream=None):
+    """Forward with the key tiles of each 256-row query block visited in ``tile_order``'s order: ``(o, lse)``.
+
+    ``tile_order``: contiguous int32 CUDA tensor ``[B, 1 or Hq, ceil(Sq/256), ceil(Sk/128)]`` of key-tile
+    indices; each row is visited in order, entries outside the block's causal tile range passed over.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-d bf16 CUDA tensor")
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if tile_order.dtype != torch.int32 or not tile_order.is_cuda or not tile_order.is_contiguous() or \
+            tile_order.dim() != 4:
+        raise ValueError("tile_order must be a contiguous 4-d int32 CUDA tensor")
+    Ho = tile_order.shape[1]
+    if tuple(tile_order.shape) != (B, Ho, -(-Sq // ORDER_ROWS), -(-Sk // ORDER_KEYS)):
+        raise ValueError(f"tile_order shape {tuple(tile_order.shape)} does not fit q{tuple(q.shape)} k{tuple(k.shape)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check(load().attn_fwd_ordered(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                   B, Hq, Hkv, Sq, Sk, D, int(causal), ctypes.c_float(scale),
+                                   tile_order.data_ptr(), int(Ho), _stream_handle(stream)))
+    return o, lse
+
+
 def bwd_workspace_size(B: int, Hq: int, Sq: int) -> int:
     return int(load("attn_bwd").attn_bwd_workspace_size(B, Hq, Sq))
 

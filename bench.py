@@ -378,6 +378,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         line["blocksparse"] = bench_blocksparse(stream, flush, dev, min(args.steps, 10))
         line["backward"] = bench_backward(stream, flush, dev, min(args.steps, 10))
         line["splitkv"] = bench_splitkv(stream, flush, dev, min(args.steps, 10))
+        line["ordered"] = bench_ordered(stream, flush, dev, min(args.steps, 10))
     if world == 1 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     return line
@@ -411,6 +412,40 @@ def bench_blocksparse(stream, flush, dev, steps: int, density: float = 0.25) -> 
         flops = 4.0 * w.D * blocksparse_pairs(w, blocks)
         out[name] = {"tflops": flops / (ts * 1e-3) / 1e12, "ms": ts, "speedup_vs_dense": td / ts,
                      "marked_fraction": float(blocks.mean())}
+    return out
+
+
+def bench_ordered(stream, flush, dev, steps: int) -> dict:
+    """Ordered forward on the gqa shape (sharply peaked rows): every 256-row query block visits its key tiles best
+    first, ranked by the dot product of block means of Q and K (a training-free priority list built outside the
+    timed region), and, as a check on the cost of the walk itself, in ascending order; both against the dense
+    kernel on the same inputs.  The work is the same as dense (every tile is visited)."""
+    from attention_forward_06_gb300 import ops
+
+    w = WORKLOADS["gqa"]
+    qx, kx, vx = [t.to(dev) for t in draw_workload(w)]
+    ox = torch.empty_like(qx)
+    lx = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    nqb, nkb = -(-w.Sq // ops.ORDER_ROWS), -(-w.Sk // ops.ORDER_KEYS)
+    with torch.no_grad():
+        qm = qx.float().reshape(w.B, w.Hq, nqb, ops.ORDER_ROWS, w.D).mean(3)
+        km = kx.float().reshape(w.B, w.Hkv, nkb, ops.ORDER_KEYS, w.D).mean(3).repeat_interleave(w.Hq // w.Hkv, 1)
+        ranked = torch.argsort(torch.einsum("bhqd,bhkd->bhqk", qm, km), dim=-1, descending=True)
+        ranked = ranked.to(torch.int32).contiguous()
+        ascending = torch.arange(nkb, dtype=torch.int32, device=dev).expand(w.B, 1, nqb, nkb).contiguous()
+    torch.cuda.synchronize()
+
+    def fd():
+        ops.attn_fwd(qx, kx, vx, causal=w.causal, scale=w.scale, o=ox, lse=lx, stream=stream)
+
+    td = statistics.mean(time_kernel(fd, steps, 3, flush, stream))
+    out = {"workload": f"{w.label()}, key tiles visited in a given order per 256-row block", "dense_ms": td}
+    for name, order in (("ranked", ranked), ("ascending", ascending)):
+        def fo():
+            ops.attn_fwd_ordered(qx, kx, vx, order, causal=w.causal, scale=w.scale, o=ox, lse=lx, stream=stream)
+
+        to = statistics.mean(time_kernel(fo, steps, 3, flush, stream))
+        out[name] = {"tflops": alg_flops(w) / (to * 1e-3) / 1e12, "ms": to, "vs_dense": td / to}
     return out
 
 

@@ -160,6 +160,39 @@ int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, f
    invalid sizes.  Host only, no CUDA call. */
 size_t attn_fwd_block_mask_words(int B, int mask_heads, int Sq, int Sk);
 
+/*
+ * Ordered forward: attn_fwd with the key tiles of every 256-row query block
+ * visited in a caller-given order.  This is the ordered-skipping kernel of page
+ * "CoSA: Accelerating Long-Context Inference via Proxy-Kernel Co-Designed Sparse
+ * Attention" (a proxy hands the kernel a priority list and the kernel reads the
+ * blocks in that order, so the most important ones come first) on the exact
+ * path: nothing is skipped that the list contains, so with a list holding every
+ * key tile the result is attention itself, the visiting order changing only the
+ * rounding of the sums.  The block of query rows [256 u, 256 u + 256) visits, in
+ * list order, every entry e of its row with 0 <= e < (its causal key-tile bound);
+ * entries outside that range are passed over.  A row that leaves a tile out makes
+ * that tile's keys invisible to the block (block-sparse attention); a tile listed
+ * twice is counted twice, so rows should list each tile at most once.
+ *
+ * tile_order: device memory, 4-byte aligned, int32 entries laid out
+ *     [B][order_heads][ceil(Sq / ATTN_ORDER_ROWS)][ceil(Sk / ATTN_ORDER_KEYS)],
+ * entry values being key-tile indices (tile kb holds keys [128 kb, 128 kb + 128)).
+ * order_heads is 1 (one order for every head) or Hq.  The order is read by the
+ * kernel and must not change until it has finished; it must not overlap o or
+ * lse.  Other arguments, layouts and status codes as attn_fwd
+ * (ATTN_ERR_INVALID_ARG also for an order_heads that is neither 1 nor Hq).  One
+ * kernel is enqueued on `stream`; nothing is allocated.
+ */
+#define ATTN_ORDER_ROWS 256
+#define ATTN_ORDER_KEYS 128
+int attn_fwd_ordered(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+                     int Sk, int D, int causal, float scale, const int32_t* tile_order, int order_heads,
+                     cudaStream_t stream);
+
+/* Number of int32 entries of a tile order for these sizes (layout above); 0 for
+   invalid sizes.  Host only, no CUDA call. */
+size_t attn_fwd_tile_order_entries(int B, int order_heads, int Sq, int Sk);
+
 /* Text for a status code.  For ATTN_ERR_CUDA it names the CUDA error of the
    calling thread's most recent failing call. */
 const char* attn_fwd_strerror(int status);

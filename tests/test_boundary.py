@@ -168,6 +168,27 @@ def test_blocksparse_invalid_arguments_before_any_device_work():
     assert args(O, 1) == ops.ATTN_ERR_INVALID_ARG       # the mask overlaps the output
 
 
+def test_tile_order_entries_formula():
+    lib = _lib.load()
+    for B, Ho, Sq, Sk in ((1, 1, 256, 128), (2, 4, 300, 5000), (1, 8, 1, 1), (3, 2, 513, 4097)):
+        assert lib.attn_fwd_tile_order_entries(B, Ho, Sq, Sk) == B * Ho * -(-Sq // 256) * -(-Sk // 128)
+    assert lib.attn_fwd_tile_order_entries(1, 0, 128, 128) == 0
+    assert lib.attn_fwd_tile_order_entries(1, 1, -1, 128) == 0
+
+
+def test_ordered_invalid_arguments_before_any_device_work():
+    lib = _lib.load()
+    T = 0x700000  # fake, aligned order address
+    args = lambda order, heads, **kw: lib.attn_fwd_ordered(Q, K, V, O, L, 1, 4, 2, 64, 64, 128, 1,
+                                                         kw.get("scale", 0.1), order, heads, None)
+    assert args(T, 3) == ops.ATTN_ERR_INVALID_ARG       # neither 1 nor Hq
+    assert args(T, 0) == ops.ATTN_ERR_INVALID_ARG
+    assert args(0, 1) == ops.ATTN_ERR_NULL_PTR
+    assert args(T + 2, 4) == ops.ATTN_ERR_MISALIGNED
+    assert args(O, 1) == ops.ATTN_ERR_INVALID_ARG       # the order overlaps the output
+    assert args(T, 1, scale=0.0) == ops.ATTN_ERR_INVALID_ARG
+
+
 def test_bwd_workspace_formula_and_invalid_arguments():
     lib = _lib.load("attn_bwd")
     for B, Hq, Sq in ((1, 1, 1), (2, 16, 2048), (3, 5, 300)):
