@@ -699,11 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       OrderWalk owalk;  // ordered mode: the same walk as the producer's
       if constexpr (ORDERED) owalk.start(order_row(p, it), p.order_len, it.n_tiles);
       for (int j = 0; j < n_tiles; ++j, ++g) {
-        ok = warp_wait(&s_full[t], g & 1, abort_v, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t r[128];
-        tmem_ld128_wait(s_tmem, r);
+        // the tile's index first (its loads overlap the wait for S)
         int jg = it.j0 + j;  // key tile index within the head
         bool own = true;     // block-sparse mode: this Q tile's query block marks the tile
         if constexpr (SPARSE) {
@@ -719,6 +715,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if constexpr (ORDERED) {
           jg = owalk.next();
         }
+        ok = warp_wait(&s_full[t], g & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r[128];
+        tmem_ld128_wait(s_tmem, r);
         // the tile is unmarked for this Q tile, or straddles the diagonal or the end of K
         const bool masked = !own || jg * BN + BN - 1 > lim_tile;
         const int kmax = own ? lim - jg * BN : -1;
