@@ -212,11 +212,19 @@ __device__ __forceinline__ uint32_t union_word(const MaskRows& m, int w, int n) 
   return u & bound_bits(w, n);
 }
 
-// number of key tiles the item visits: the marked tiles within its causal bound
+// number of key tiles the item visits: the marked tiles within its causal bound (the
+// lanes of the calling warp take one word each)
 __device__ __forceinline__ int sparse_tiles(const Params& p, const Item& it) {
   const MaskRows m = mask_rows(p, it);
+  const int lane = static_cast<int>(threadIdx.x % 32);
   int n = 0;
-  for (int w = 0; w * 32 < it.n_tiles; ++w) n += __popc(union_word(m, w, it.n_tiles));
+  for (int w0 = 0; w0 * 32 < it.n_tiles; w0 += 32) {
+    const int w = w0 + lane;
+    int c = w * 32 < it.n_tiles ? __popc(union_word(m, w, it.n_tiles)) : 0;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+    n += c;
+  }
   return n;
 }
 
@@ -242,11 +250,22 @@ __device__ __forceinline__ uint32_t order_window(const int32_t* row, int len, in
   return __ballot_sync(0xffffffffu, val >= 0 && val < n);
 }
 
-// number of key tiles an item visits in ordered mode (the whole warp calls it)
+// number of key tiles an item visits in ordered mode (the whole warp calls it; four
+// windows' loads are in flight together)
 __device__ __forceinline__ int ordered_tiles(const Params& p, const Item& it) {
   const int32_t* row = order_row(p, it);
-  int n = 0, v;
-  for (int w = 0; 32 * w < p.order_len; ++w) n += __popc(order_window(row, p.order_len, w, it.n_tiles, v));
+  const int lane = static_cast<int>(threadIdx.x % 32);
+  int n = 0;
+  for (int w0 = 0; 32 * w0 < p.order_len; w0 += 4) {
+    int v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = 32 * (w0 + u) + lane;
+      v[u] = e < p.order_len ? __ldg(row + e) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) n += __popc(__ballot_sync(0xffffffffu, v[u] >= 0 && v[u] < it.n_tiles));
+  }
   return n;
 }
 
