@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __nv_bfloat16*
     nlse2[row] = nl2;
     ndelta[row] = -acc;
   }
+  griddep_launch_dependents();  // the dK/dV kernel may start its set-up
 }
 
 // The k-th work item of this CTA.  Items are listed heaviest first and dealt in
@@ -218,6 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
    regs_decrease<kRegsOther>();
    if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
+    // The prep kernel's vectors are complete before the first load; then the dQ
+    // kernel may be scheduled (its CTAs take the SMs this kernel's CTAs leave).
+    griddep_wait();
+    griddep_launch_dependents();
     uint32_t it = 0, n_ne = 0;  // ring loads issued; items with query tiles
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
@@ -713,6 +718,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // this grid may run beside the tail of the dK/dV kernel (it reads only the prep
+  // kernel's vectors, complete before the dK/dV kernel let it start); it completes
+  // after that kernel, so work later in the stream sees all three gradients
+  if (threadIdx.x == 0) griddep_wait();
 }
 
 // ----------------------------------------------------------------------------
@@ -778,17 +787,26 @@ int launch_all(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
       o, dout, lse, lse2, delta, prm.BH, prm.Sq, prm.Sq_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
+  // the dK/dV and dQ kernels are launched with programmatic stream serialisation: each
+  // may be scheduled before the previous kernel has finished (see griddep_* in ptx.cuh)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = BCfg<D>::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   BParams a = prm;
   a.n_items = prm.n_kt * prm.BZ;
-  attn_bwd_dkdv_kernel<D><<<a.n_items < sms ? a.n_items : sms, kThreads, BCfg<D>::kSmemBytes, stream>>>(tq, tk, tv,
-                                                                                                     tdo, a);
-  e = cudaGetLastError();
+  cfg.gridDim = dim3(a.n_items < sms ? a.n_items : sms);
+  e = cudaLaunchKernelEx(&cfg, attn_bwd_dkdv_kernel<D>, tq, tk, tv, tdo, a);
   if (e != cudaSuccess) return cuda_fail(e);
   BParams b = prm;
   b.n_items = prm.n_qt * prm.BH;
-  attn_bwd_dq_kernel<D><<<b.n_items < sms ? b.n_items : sms, kThreads, BCfg<D>::kSmemBytes, stream>>>(tq, tk, tv,
-                                                                                                   tdo, b);
-  e = cudaGetLastError();
+  cfg.gridDim = dim3(b.n_items < sms ? b.n_items : sms);
+  e = cudaLaunchKernelEx(&cfg, attn_bwd_dq_kernel<D>, tq, tk, tv, tdo, b);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 

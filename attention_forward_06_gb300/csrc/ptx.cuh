@@ -189,6 +189,16 @@ __device__ __forceinline__ void bulk_wait_group0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Programmatic dependent launch.  griddep_wait: wait until the grids this one depends
+// on (the previous kernel of the stream, when launched with programmatic stream
+// serialisation) have completed and their memory operations are visible.
+// griddep_launch_dependents: let the next such kernel be scheduled once every CTA
+// of this grid has signalled or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
