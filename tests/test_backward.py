@@ -106,3 +106,32 @@ def test_deterministic_bitwise():
     b = ops.attn_bwd(q, k, v, o, lse, do, causal=1)
     torch.cuda.synchronize()
     assert all(torch.equal(x, y) for x, y in zip(a, b))
+
+
+def test_back_to_back_calls_on_two_streams():
+    """The three backward kernels overlap one another (programmatic dependent launch):
+    many calls in a row, alternating two streams and two shapes, each read right after
+    its stream's work, must all reproduce the first result of their shape bit for bit."""
+    shapes = [(2, 4, 2, 500, 700, 128, 1), (1, 8, 8, 1024, 1024, 64, 0)]
+    data = []
+    for (B, Hq, Hkv, Sq, Sk, D, causal) in shapes:
+        q, k, v = [t.cuda() for t in draw(B, Hq, Hkv, Sq, Sk, D, seed=Sq + D)]
+        do = draw(B, Hq, Hkv, Sq, Sk, D, seed=Sq + D + 1)[0].cuda()
+        o, lse = ops.attn_fwd(q, k, v, causal=causal)
+        data.append((q, k, v, o, lse, do, causal))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    first = {}
+    for i in range(24):
+        s = streams[i % 2]
+        q, k, v, o, lse, do, causal = data[(i // 2) % 2]
+        with torch.cuda.stream(s):
+            got = ops.attn_bwd(q, k, v, o, lse, do, causal=causal, stream=s)
+            host = [t.cpu() for t in got]  # synchronous copies on the same stream
+        st, site = ops.bwd_debug_status(s)
+        assert st == ops.ATTN_OK, f"backward wait ran out at site {site}"
+        key = (i // 2) % 2
+        if key not in first:
+            first[key] = host
+        else:
+            assert all(torch.equal(x, y) for x, y in zip(first[key], host)), i
