@@ -734,14 +734,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if constexpr (ORDERED) {
           jg = owalk.next();
         }
-        ok = warp_wait(&s_full[t], g & 1, abort_v, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t r[128];
-        tmem_ld128_wait(s_tmem, r);
         // the tile is unmarked for this Q tile, or straddles the diagonal or the end of K
         const bool masked = !own || jg * BN + BN - 1 > lim_tile;
         const int kmax = own ? lim - jg * BN : -1;
+        ok = warp_wait(&s_full[t], g & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        if constexpr (SPARSE) {
+          // block-sparse mode: a tile no row of this warp sees (one only the other Q tile's
+          // query block marks, or one past this tile's causal limit) has P = 0, written
+          // without reading S or taking an exponential
+          if (__all_sync(0xffffffffu, kmax < 0)) {
+            uint32_t z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0u;
+            tmem_st32(s_tmem + 64, z);
+            tmem_st32(s_tmem + 96, z);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_full[t]);
+            continue;
+          }
+        }
+        uint32_t r[128];
+        tmem_ld128_wait(s_tmem, r);
         if (masked) {
 #pragma unroll
           for (int i = 0; i < 128; ++i) r[i] = (i > kmax) ? __float_as_uint(-INFINITY) : r[i];
