@@ -478,12 +478,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       OrderWalk owalk;  // ordered mode: the item's row of the order
       if constexpr (ORDERED) owalk.start(order_row(p, it), p.order_len, it.n_tiles);
       for (int i = 0; i < 2 * n_tiles; ++i) {  // K_j is load 2j, V_j is load 2j+1
-        if (k == 0 && i == 2) {
-          // all CTAs start at once: let the first item's Q and K_0 land before streaming
-          // more, so they are not queued behind the rest of the start-up burst in DRAM
-          ok = warp_wait(&q_full, 0, abort_v, kTimeoutNs) && warp_wait(&kv_full[0], 0, abort_v, kTimeoutNs);
-          if (!ok) break;
-        }
         const uint32_t slot = kv_it % S;
         const uint32_t use = kv_it / S;
         if (use > 0) {
