@@ -18,11 +18,12 @@
 //                          form, A from TMEM) accumulate in TMEM across the whole item
 //   attn_bwd_dq_kernel     one (batch, query head, 128-row tile) per item: S = Q K^T,
 //                          dP = dO V^T, dS into TMEM, dQ += dS K
-// Each kernel takes a step (a 128-row query tile, or a 128-key tile) in two 64-wide
-// halves held in two TMEM regions; warpgroup r (warps 4r .. 4r+3, one thread per TMEM
-// lane) computes half r while the tensor cores run the other half's products.  Warp 8
-// loads with TMA, warp 9 issues the tcgen05 MMAs, warps 10-11 idle; every wait is
-// bounded as in the forward.
+// The dK/dV kernel takes a step (a 128-row query tile) in two 64-wide halves held in
+// two TMEM regions, warpgroup r (warps 4r .. 4r+3, one thread per TMEM lane) computing
+// half r while the tensor cores run the other half's products; the dQ kernel computes a
+// step's S and dP 128 keys wide, alternating two S regions, and its warpgroups split
+// the keys.  Warp 8 loads with TMA, warp 9 issues the tcgen05 MMAs, warps 10-11 idle;
+// every wait is bounded as in the forward.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,7 +41,7 @@ using namespace attn;
 namespace {
 
 constexpr int BT = 128;  // query rows / keys per tile (MMA M)
-constexpr int BH2 = 64;  // rows (dK/dV) or keys (dQ) of one half step (MMA N of the S-type products)
+constexpr int BH2 = 64;  // query rows of a half step (dK/dV: MMA N of S^T, dP^T), keys per warpgroup (dQ)
 constexpr int kHalfBytes = BH2 * 128;  // byte offset of a tile's second half of rows in a 128-B-swizzled block
 constexpr int kThreads = 384;          // three warpgroups
 constexpr int kComputeWarps = 8;       // warpgroup r computes half r of every step
@@ -50,7 +51,7 @@ constexpr uint32_t kRegsLaunch = 168;   // 65536 / 384
 constexpr uint32_t kRegsCompute = 224;  // warpgroups 0 and 1
 constexpr uint32_t kRegsOther = 56;     // warpgroup 2
 static_assert(256 * kRegsCompute + 128 * kRegsOther <= kThreads * kRegsLaunch, "register split exceeds the pool");
-constexpr int kRing = 2;  // streamed tile-pair slots
+constexpr int kRing = 2;  // streamed Q/dO tile-pair slots of the dK/dV kernel
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 constexpr uint64_t kDrainTimeoutNs = 500000000ull;
@@ -470,37 +471,59 @@ __device__ __forceinline__ int key_tiles(const BParams& p, int i) {
 
 // ---------------------------------------------------------------------------- dQ
 // Work item x: query tile i = n_qt - 1 - x / (B*Hq) (heaviest first under a causal
-// mask), slice bh = x % (B*Hq).  A step is one 128-key tile, taken in two halves of
-// 64 keys; half r lives in TMEM region r (lane = query row): S_r at columns
-// [128 r, 128 r + 64), dP_r at [128 r + 64, 128 r + 128), dS_r (bf16 pairs) over the
-// first 32 columns of S_r; dQ [256, 256 + D) accumulates over the item.  Compute
-// warpgroup r owns half r, as in the dK/dV kernel.
+// mask), slice bh = x % (B*Hq).  A step is one 128-key tile.  S = Q K^T of a step goes
+// to one of two TMEM regions (steps alternate: [0,128) and [128,256)), dP = dO V^T to
+// [256,384), dQ accumulates at [384, 384 + D) (lane = query row); both products are 128
+// wide (a 64-wide product costs half again as many tensor cycles per FLOP).  Warpgroup r
+// takes keys 64 r .. 64 r + 63 of every step and writes their dS (bf16 pairs) over its
+// own S columns [64 r, 64 r + 32) of the step's region.  The next step's S and dP go in
+// as soon as both warpgroups have read this step's dP, so the tensor cores compute them
+// while the warpgroups work; K streams through a three-slot ring (it is read again by
+// dQ += dS K) and V through a two-slot one.  Each warpgroup's dS-ready barrier is
+// doubled by step parity so it can never get two phases ahead of the issuer.
+template <int D>
+struct QCfg {
+  static constexpr int kTileBytes = BT * D * 2;
+  static constexpr int kKRing = 3, kVRing = 2;
+  static constexpr int kSmemBytes = (2 + kKRing + kVRing) * kTileBytes + 1024;  // Q, dO, K ring, V ring
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                        const BParams p) {
-  using C = BCfg<D>;
+  using C = QCfg<D>;
+  using BC = BCfg<D>;
+  constexpr int KR = C::kKRing, VR = C::kVRing;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint8_t* q_s = smem;
   uint8_t* do_s = smem + C::kTileBytes;
-  uint8_t* ring = smem + 2 * C::kTileBytes;  // slot: K, V
-  __shared__ uint64_t qd_full, qd_empty, full[kRing], empty[kRing], st_full[2], ds_full[2], acc_full, acc_empty,
-      drain;
+  uint8_t* k_ring = smem + 2 * C::kTileBytes;
+  uint8_t* v_ring = k_ring + KR * C::kTileBytes;
+  __shared__ uint64_t qd_full, qd_empty, kfull[KR], kempty[KR], vfull[VR], vempty[VR], st_full, dp_free,
+      ds_full[2][2], acc_full, acc_empty, drain;
   __shared__ uint32_t tmem_slot, abort_flag;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
     mbar_init(&qd_full, 1);
     mbar_init(&qd_empty, 1);
-    for (int s = 0; s < kRing; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < KR; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
     }
+    for (int s = 0; s < VR; ++s) {
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
+    }
+    mbar_init(&st_full, 1);
+    mbar_init(&dp_free, kComputeWarps * 32);
     for (int r = 0; r < 2; ++r) {
-      mbar_init(&st_full[r], 1);
-      mbar_init(&ds_full[r], 128);
+      mbar_init(&ds_full[r][0], 128);
+      mbar_init(&ds_full[r][1], 128);
     }
     mbar_init(&acc_full, 1);
     mbar_init(&acc_empty, kComputeWarps * 32);
@@ -522,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
    regs_decrease<kRegsOther>();
    if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
-    uint32_t it = 0, n_ne = 0;
+    uint32_t kl = 0, vl = 0, n_ne = 0;  // K and V tiles loaded; items with key tiles
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
       const int x = item_of(k);
@@ -535,106 +558,120 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx_elect(&qd_full, 2 * C::kTileBytes);
 #pragma unroll
       for (int cb = 0; cb < D / 64; ++cb) {
-        tma_load_3d_elect(q_s + cb * C::kColBlockBytes, &tq, &qd_full, cb * 64, i * BT, bh);
-        tma_load_3d_elect(do_s + cb * C::kColBlockBytes, &tdo, &qd_full, cb * 64, i * BT, bh);
+        tma_load_3d_elect(q_s + cb * BC::kColBlockBytes, &tq, &qd_full, cb * 64, i * BT, bh);
+        tma_load_3d_elect(do_s + cb * BC::kColBlockBytes, &tdo, &qd_full, cb * 64, i * BT, bh);
       }
       ++n_ne;
       const int kvz = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.G;
-      for (int j = 0; j < n && ok; ++j, ++it) {
-        const uint32_t slot = it % kRing, use = it / kRing;
-        if (use > 0) ok = warp_wait(&empty[slot], (use - 1) & 1, abort_v, kTimeoutNs);
+      for (int j = 0; j < n && ok; ++j, ++kl, ++vl) {
+        const uint32_t ks = kl % KR, vs = vl % VR;
+        if (kl >= KR) ok = warp_wait(&kempty[ks], (kl / KR - 1) & 1, abort_v, kTimeoutNs);
         if (!ok) break;
-        uint8_t* sl = ring + slot * C::kSlotBytes;
-        mbar_arrive_expect_tx_elect(&full[slot], 2 * C::kTileBytes);
+        mbar_arrive_expect_tx_elect(&kfull[ks], C::kTileBytes);
 #pragma unroll
-        for (int cb = 0; cb < D / 64; ++cb) {
-          tma_load_3d_elect(sl + cb * C::kColBlockBytes, &tk, &full[slot], cb * 64, j * BT, kvz);
-          tma_load_3d_elect(sl + C::kTileBytes + cb * C::kColBlockBytes, &tv, &full[slot], cb * 64, j * BT, kvz);
+        for (int cb = 0; cb < D / 64; ++cb)
+          tma_load_3d_elect(k_ring + ks * C::kTileBytes + cb * BC::kColBlockBytes, &tk, &kfull[ks], cb * 64, j * BT,
+                            kvz);
+        if (vl >= VR) ok = warp_wait(&vempty[vs], (vl / VR - 1) & 1, abort_v, kTimeoutNs);
+        if (!ok) {
+          ++kl;  // the K tile above is in flight
+          break;
         }
+        mbar_arrive_expect_tx_elect(&vfull[vs], C::kTileBytes);
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb)
+          tma_load_3d_elect(v_ring + vs * C::kTileBytes + cb * BC::kColBlockBytes, &tv, &vfull[vs], cb * 64, j * BT,
+                            kvz);
       }
     }
     if (!ok) {
       if (lane == 0) record_abort(abort_v, kSiteProducer);
-      for (uint32_t u = (it > kRing ? it - kRing : 0); u < it; ++u)
-        mbar_wait_bounded(&full[u % kRing], (u / kRing) & 1, abort_v, kDrainTimeoutNs);
+      for (uint32_t u = (kl > KR ? kl - KR : 0); u < kl; ++u)
+        mbar_wait_bounded(&kfull[u % KR], (u / KR) & 1, abort_v, kDrainTimeoutNs);
+      for (uint32_t u = (vl > VR ? vl - VR : 0); u < vl; ++u)
+        mbar_wait_bounded(&vfull[u % VR], (u / VR) & 1, abort_v, kDrainTimeoutNs);
       if (n_ne > 0) mbar_wait_bounded(&qd_full, (n_ne - 1) & 1, abort_v, kDrainTimeoutNs);
     }
    } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tcgen05 issuer
-    constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BH2, false);  // M = 128 rows, N = 64 keys
-    constexpr uint32_t idesc_acc = idesc_bf16_f32(BT, D, true);   // M = 128 rows, N = D, B MN-major
-    const uint32_t q_addr = smem_u32(q_s), do_addr = smem_u32(do_s), ring_addr = smem_u32(ring);
-    // S_r = Q K_r^T and dP_r = dO V_r^T for half r of the key tile in ring slot `slot`
-    auto issue_s = [&](int r, uint32_t slot) {
-      const uint32_t k_addr = opaque(ring_addr) + slot * C::kSlotBytes + r * kHalfBytes;
+    constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, false);  // M = 128 rows, N = 128 keys
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(BT, D, true);  // M = 128 rows, N = D, B MN-major
+    constexpr uint32_t kDp = 2 * BT, kDq = 3 * BT;               // TMEM columns of dP and dQ
+    const uint32_t q_addr = smem_u32(q_s), do_addr = smem_u32(do_s);
+    const uint32_t k_addr = smem_u32(k_ring), v_addr = smem_u32(v_ring);
+    // S = Q K^T into TMEM region `reg` and dP = dO V^T; V is free once dP is done
+    auto issue_s = [&](uint32_t reg, uint32_t ks, uint32_t vs) {
       const uint64_t qd = sdesc_sw128(q_addr, 16, 1024), dod = sdesc_sw128(do_addr, 16, 1024);
-      const uint64_t kd = sdesc_sw128(k_addr, 16, 1024), vd = sdesc_sw128(k_addr + C::kTileBytes, 16, 1024);
+      const uint64_t kd = sdesc_sw128(opaque(k_addr) + ks * C::kTileBytes, 16, 1024);
+      const uint64_t vd = sdesc_sw128(opaque(v_addr) + vs * C::kTileBytes, 16, 1024);
       if constexpr (D == 128) {
-        mma_bf16_ss_k8(tmem + 128 * r, qd, kd, idesc_s);
-        mma_bf16_ss_k8(tmem + 128 * r + BH2, dod, vd, idesc_s, smem_u32(&st_full[r]));
+        mma_bf16_ss_k8(tmem + reg, qd, kd, idesc_s);
+        mma_bf16_ss_k8(tmem + kDp, dod, vd, idesc_s, smem_u32(&st_full), smem_u32(&vempty[vs]));
       } else {
-        mma_bf16_ss_k4(tmem + 128 * r, qd, kd, idesc_s);
-        mma_bf16_ss_k4(tmem + 128 * r + BH2, dod, vd, idesc_s, smem_u32(&st_full[r]));
+        mma_bf16_ss_k4(tmem + reg, qd, kd, idesc_s);
+        mma_bf16_ss_k4(tmem + kDp, dod, vd, idesc_s, smem_u32(&st_full), smem_u32(&vempty[vs]));
       }
     };
-    // dQ += dS_r K_r: A (dS_r) from TMEM, B (K_r) MN-major over the half's 64 keys
-    auto issue_acc = [&](int r, uint32_t slot, uint32_t acc, uint32_t bar0, uint32_t bar1) {
-      const uint32_t k_addr = opaque(ring_addr) + slot * C::kSlotBytes + r * kHalfBytes;
-      const uint64_t kb = sdesc_sw128(k_addr, C::kColBlockBytes, 1024);
-      mma_bf16_ts_k4(tmem + 2 * BT, tmem + 128 * r, kb, idesc_acc, acc, bar0, bar1);
+    // dQ += dS K for step gg (dS in region gg & 1, K in slot ks), one 64-key half per
+    // warpgroup as its dS arrives; the item's first step overwrites dQ once the previous
+    // item's epilogue has read it, its last commits acc_full; K is free afterwards
+    auto issue_acc = [&](uint32_t gg, uint32_t ks, bool first, bool last, uint32_t tt) -> bool {
+      const uint32_t reg = tmem + BT * (gg & 1), ka = opaque(k_addr) + ks * C::kTileBytes;
+      bool w = warp_wait(&ds_full[0][gg & 1], (gg >> 1) & 1, abort_v, kTimeoutNs);
+      if (w && first && tt > 0) w = warp_wait(&acc_empty, (tt - 1) & 1, abort_v, kTimeoutNs);
+      if (!w) return false;
+      tc_fence_after();
+      mma_bf16_ts_k4(tmem + kDq, reg, sdesc_sw128(ka, BC::kColBlockBytes, 1024), idesc_acc, first ? 0u : 1u);
+      w = warp_wait(&ds_full[1][gg & 1], (gg >> 1) & 1, abort_v, kTimeoutNs);
+      if (!w) return false;
+      tc_fence_after();
+      mma_bf16_ts_k4(tmem + kDq, reg + BH2, sdesc_sw128(ka + kHalfBytes, BC::kColBlockBytes, 1024), idesc_acc, 1u,
+                     smem_u32(&kempty[ks]), last ? smem_u32(&acc_full) : kNoBar);
+      return true;
     };
-    uint32_t it = 0, g = 0, n_ne = 0;
+    // Order on the tensor pipe: S(g) dP(g) dQ+=(g-1) S(g+1) dP(g+1) dQ+=(g) ..., across items too
+    uint32_t g = 0, t = 0;    // steps (= K and V tiles), items with key tiles
+    uint32_t pk = 0, pt = 0;  // the step whose dQ += dS K is pending: K slot, item
+    int pj = -1, pn = 0;      // ... and its index within the item, the item's steps
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
       const int x = item_of(k);
       if (x >= p.n_items) continue;
       const int n = key_tiles(p, p.n_qt - 1 - x / p.BH);
       if (n <= 0) continue;
-      ok = warp_wait(&qd_full, n_ne & 1, abort_v, kTimeoutNs);
-      if (ok) ok = warp_wait(&full[it % kRing], (it / kRing) & 1, abort_v, kTimeoutNs);
-      if (!ok) break;
-      tc_fence_after();
-      issue_s(0, it % kRing);
-      issue_s(1, it % kRing);
-      // Q and dO are read only by the S-type products (see the dK/dV kernel)
-      if (n == 1) mma_commit_elect(&qd_empty);
-      for (int j = 0; j < n; ++j, ++it, ++g) {
-        const uint32_t slot = it % kRing, next = (it + 1) % kRing;
-        const bool more = j + 1 < n;
-        ok = warp_wait(&ds_full[0], g & 1, abort_v, kTimeoutNs);
-        if (ok && j == 0 && n_ne > 0) ok = warp_wait(&acc_empty, (n_ne - 1) & 1, abort_v, kTimeoutNs);
+      ok = warp_wait(&qd_full, t & 1, abort_v, kTimeoutNs);
+      for (int j = 0; j < n && ok; ++j, ++g) {
+        const uint32_t ks = g % KR, vs = g % VR;
+        if (g > 0) ok = warp_wait(&dp_free, (g - 1) & 1, abort_v, kTimeoutNs);  // dP(g-1) read by all
+        if (ok) ok = warp_wait(&kfull[ks], (g / KR) & 1, abort_v, kTimeoutNs);
+        if (ok) ok = warp_wait(&vfull[vs], (g / VR) & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        issue_acc(0, slot, j > 0 ? 1u : 0u, kNoBar, kNoBar);
-        if (more) {
-          ok = warp_wait(&full[next], ((it + 1) / kRing) & 1, abort_v, kTimeoutNs);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(0, next);
-        }
-        ok = warp_wait(&ds_full[1], g & 1, abort_v, kTimeoutNs);
-        if (!ok) break;
-        tc_fence_after();
-        issue_acc(1, slot, 1u, smem_u32(&empty[slot]), more ? kNoBar : smem_u32(&acc_full));
-        if (more) issue_s(1, next);
-        if (j + 2 == n) mma_commit_elect(&qd_empty);  // that was the item's last S-type pair
+        issue_s(BT * (g & 1), ks, vs);
+        if (j + 1 == n) mma_commit_elect(&qd_empty);  // Q and dO are read only by S and dP
+        if (pj >= 0) ok = issue_acc(g - 1, pk, pj == 0, pj + 1 == pn, pt);
+        pk = ks;
+        pj = j;
+        pn = n;
+        pt = t;
       }
       if (!ok) break;
-      ++n_ne;
+      ++t;
     }
+    if (ok && pj >= 0) ok = issue_acc(g - 1, pk, pj == 0, pj + 1 == pn, pt);
     if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
     mma_commit_elect(&drain);
     warp_wait(&drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
    }
   } else {
     // ------------------------------------------------------------ compute (one thread per query row)
-    // Warpgroup r takes half r (keys 64 r .. 64 r + 63) of every key tile; at the end of an
-    // item it writes columns r * D/2 .. of the row's dQ.
+    // Warpgroup r takes keys 64 r .. 64 r + 63 of every key tile; at the end of an item it
+    // writes columns r * D/2 .. of the row's dQ.
     regs_increase<kRegsCompute>();
     const int r = warp / 4, quarter = warp % 4;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t s_t = tmem + lane_off + 128 * r, dp_t = s_t + BH2, dq_t = tmem + lane_off + 2 * BT;
-    uint32_t g = 0, n_ne = 0;
+    const uint32_t dp_t = tmem + lane_off + 2 * BT + BH2 * r, dq_t = tmem + lane_off + 3 * BT;
+    uint32_t g = 0, t = 0;
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
       const int x = item_of(k);
@@ -657,11 +694,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t c2 = f2_pack(p.c, p.c), nl2 = f2_pack(nl, nl), nd2 = f2_pack(nd, nd);
       const int lim = p.causal ? min(p.Sk - 1, row + p.diag) : p.Sk - 1;  // last visible key
       for (int j = 0; j < n; ++j, ++g) {
-        ok = warp_wait(&st_full[r], g & 1, abort_v, kTimeoutNs);
+        ok = warp_wait(&st_full, g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t s_t = tmem + lane_off + BT * (g & 1) + BH2 * r;
         uint32_t sv[64], dpv[64];
         tmem_ld2x64_wait(s_t, dp_t, sv, dpv);
+        tc_fence_before();
+        mbar_arrive(&dp_free);  // the next step's S and dP may go in
         // keys past kmax (above the diagonal, or past Sk) get S = -inf, hence P = 0 (c > 0)
         const int kmax = lim - j * BT - BH2 * r;
         if (__any_sync(0xffffffffu, kmax < BH2 - 1)) {
@@ -682,12 +722,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(s_t, dsk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&ds_full[r]);
+        mbar_arrive(&ds_full[r][g & 1]);
       }
       if (!ok) break;
-      ok = warp_wait(&acc_full, n_ne & 1, abort_v, kTimeoutNs);
+      ok = warp_wait(&acc_full, t & 1, abort_v, kTimeoutNs);
       if (!ok) break;
-      ++n_ne;
+      ++t;
       tc_fence_after();
 #pragma unroll
       for (int cb = 0; cb < D / 64; ++cb) {
@@ -758,7 +798,7 @@ int prepare_device(int dev) {
                        reinterpret_cast<const void*>(attn_bwd_dq_kernel<128>),
                        reinterpret_cast<const void*>(attn_bwd_dkdv_kernel<64>),
                        reinterpret_cast<const void*>(attn_bwd_dq_kernel<64>)};
-  const int bytes[] = {BCfg<128>::kSmemBytes, BCfg<128>::kSmemBytes, BCfg<64>::kSmemBytes, BCfg<64>::kSmemBytes};
+  const int bytes[] = {BCfg<128>::kSmemBytes, QCfg<128>::kSmemBytes, BCfg<64>::kSmemBytes, QCfg<64>::kSmemBytes};
   for (int f = 0; f < 4 && e == cudaSuccess; ++f)
     e = cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes[f]);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -806,6 +846,7 @@ int launch_all(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
   BParams b = prm;
   b.n_items = prm.n_qt * prm.BH;
   cfg.gridDim = dim3(b.n_items < sms ? b.n_items : sms);
+  cfg.dynamicSmemBytes = QCfg<D>::kSmemBytes;
   e = cudaLaunchKernelEx(&cfg, attn_bwd_dq_kernel<D>, tq, tk, tv, tdo, b);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
