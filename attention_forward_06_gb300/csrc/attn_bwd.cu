@@ -599,18 +599,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kDp = 2 * BT, kDq = 3 * BT;               // TMEM columns of dP and dQ
     const uint32_t q_addr = smem_u32(q_s), do_addr = smem_u32(do_s);
     const uint32_t k_addr = smem_u32(k_ring), v_addr = smem_u32(v_ring);
-    // S = Q K^T into TMEM region `reg` and dP = dO V^T; V is free once dP is done
-    auto issue_s = [&](uint32_t reg, uint32_t ks, uint32_t vs) {
-      const uint64_t qd = sdesc_sw128(q_addr, 16, 1024), dod = sdesc_sw128(do_addr, 16, 1024);
+    // S = Q K^T into TMEM region `reg`
+    auto issue_s = [&](uint32_t reg, uint32_t ks) {
+      const uint64_t qd = sdesc_sw128(q_addr, 16, 1024);
       const uint64_t kd = sdesc_sw128(opaque(k_addr) + ks * C::kTileBytes, 16, 1024);
-      const uint64_t vd = sdesc_sw128(opaque(v_addr) + vs * C::kTileBytes, 16, 1024);
-      if constexpr (D == 128) {
+      if constexpr (D == 128)
         mma_bf16_ss_k8(tmem + reg, qd, kd, idesc_s);
-        mma_bf16_ss_k8(tmem + kDp, dod, vd, idesc_s, smem_u32(&st_full), smem_u32(&vempty[vs]));
-      } else {
+      else
         mma_bf16_ss_k4(tmem + reg, qd, kd, idesc_s);
+    };
+    // dP = dO V^T; the step's S and dP are then ready, and V is free
+    auto issue_dp = [&](uint32_t vs) {
+      const uint64_t dod = sdesc_sw128(do_addr, 16, 1024);
+      const uint64_t vd = sdesc_sw128(opaque(v_addr) + vs * C::kTileBytes, 16, 1024);
+      if constexpr (D == 128)
+        mma_bf16_ss_k8(tmem + kDp, dod, vd, idesc_s, smem_u32(&st_full), smem_u32(&vempty[vs]));
+      else
         mma_bf16_ss_k4(tmem + kDp, dod, vd, idesc_s, smem_u32(&st_full), smem_u32(&vempty[vs]));
-      }
     };
     // dQ += dS K for step gg (dS in region gg & 1, K in slot ks), one 64-key half per
     // warpgroup as its dS arrives; the item's first step overwrites dQ once the previous
@@ -629,7 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                      smem_u32(&kempty[ks]), last ? smem_u32(&acc_full) : kNoBar);
       return true;
     };
-    // Order on the tensor pipe: S(g) dP(g) dQ+=(g-1) S(g+1) dP(g+1) dQ+=(g) ..., across items too
+    // Order on the tensor pipe: S(g) dP(g) dQ+=(g-1) S(g+1) dP(g+1) dQ+=(g) ..., across items too.
+    // S(g) overwrites step g-2's region, whose S was read before dP(g-1) went in and whose dS
+    // was consumed by the products issued before it, so it is issued without waiting for the
+    // warpgroups; only dP(g) waits for them to have read dP(g-1).
     uint32_t g = 0, t = 0;    // steps (= K and V tiles), items with key tiles
     uint32_t pk = 0, pt = 0;  // the step whose dQ += dS K is pending: K slot, item
     int pj = -1, pn = 0;      // ... and its index within the item, the item's steps
@@ -642,12 +650,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait(&qd_full, t & 1, abort_v, kTimeoutNs);
       for (int j = 0; j < n && ok; ++j, ++g) {
         const uint32_t ks = g % KR, vs = g % VR;
+        ok = warp_wait(&kfull[ks], (g / KR) & 1, abort_v, kTimeoutNs);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(BT * (g & 1), ks);
         if (g > 0) ok = warp_wait(&dp_free, (g - 1) & 1, abort_v, kTimeoutNs);  // dP(g-1) read by all
-        if (ok) ok = warp_wait(&kfull[ks], (g / KR) & 1, abort_v, kTimeoutNs);
         if (ok) ok = warp_wait(&vfull[vs], (g / VR) & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
-        issue_s(BT * (g & 1), ks, vs);
+        issue_dp(vs);
         if (j + 1 == n) mma_commit_elect(&qd_empty);  // Q and dO are read only by S and dP
         if (pj >= 0) ok = issue_acc(g - 1, pk, pj == 0, pj + 1 == pn, pt);
         pk = ks;
