@@ -48,9 +48,12 @@ constexpr int kComputeWarps = 8;       // warpgroup r computes half r of every s
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;            // warps 10 and 11 idle (they complete the third warpgroup)
 constexpr uint32_t kRegsLaunch = 168;   // 65536 / 384
-constexpr uint32_t kRegsCompute = 224;  // warpgroups 0 and 1
-constexpr uint32_t kRegsOther = 56;     // warpgroup 2
+constexpr uint32_t kRegsCompute = 224;  // dQ kernel: warpgroups 0 and 1 ...
+constexpr uint32_t kRegsOther = 56;     // ... and warpgroup 2
 static_assert(256 * kRegsCompute + 128 * kRegsOther <= kThreads * kRegsLaunch, "register split exceeds the pool");
+// dK/dV kernel: its producer and issuer spill at 56 registers (ptxas) with the epilogue's shuffles
+constexpr uint32_t kRegsComputeKV = 216, kRegsOtherKV = 72;
+static_assert(256 * kRegsComputeKV + 128 * kRegsOtherKV <= kThreads * kRegsLaunch, "register split exceeds the pool");
 constexpr int kRing = 2;  // streamed Q/dO tile-pair slots of the dK/dV kernel
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
@@ -98,6 +101,41 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 __device__ __forceinline__ void record_abort(volatile uint32_t* abort_flag, int site) {
   *abort_flag = 1;
   atomicCAS(&g_bwd_status, 0, site);
+}
+
+// Stores 32 rows of a warp, one row per lane (lane m holds its row's CH 16-byte chunks in
+// w[0 .. 4 CH)), row m at base + m * stride; rows m >= live_rows are skipped.  A warp store
+// of one 16-byte chunk per lane would touch 32 rows (32 cache lines); instead the chunks are
+// transposed within each group of CH lanes (log2 CH butterfly stages of shuffles, each
+// swapping one bit between lane and chunk index), after which lane CH g + q holds chunk q of
+// rows CH g .. CH g + CH - 1, and each of the CH stores writes 32 / CH whole rows.
+template <int CH>
+__device__ __forceinline__ void store_warp_rows(uint32_t (&w)[4 * CH], uint8_t* base, int64_t stride, int live_rows,
+                                                int lane) {
+  const int q = lane % CH;
+#pragma unroll
+  for (int b = CH / 2; b >= 1; b /= 2) {
+    const bool hi = (q & b) != 0;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      if (c & b) continue;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const uint32_t send = hi ? w[4 * c + h] : w[4 * (c ^ b) + h];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, b);
+        if (hi)
+          w[4 * c + h] = recv;
+        else
+          w[4 * (c ^ b) + h] = recv;
+      }
+    }
+  }
+  const int m0 = lane - q;
+#pragma unroll
+  for (int k = 0; k < CH; ++k)
+    if (m0 + k < live_rows)
+      *reinterpret_cast<uint4*>(base + (m0 + k) * stride + 16 * q) =
+          make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
 // ---------------------------------------------------------------------------- prep
@@ -217,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.G;
 
   if (warp >= 8) {
-   regs_decrease<kRegsOther>();
+   regs_decrease<kRegsOtherKV>();
    if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
     // The prep kernel's vectors are complete before the first load; then the dQ
@@ -348,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // key kk reads its lane of S^T_r and dP^T_r (64 columns each) and writes P^T_r and
     // dS^T_r over their first 32 columns, its own lane only.  At the end of an item
     // warpgroup 0 writes dV, warpgroup 1 scale * dK.
-    regs_increase<kRegsCompute>();
+    regs_increase<kRegsComputeKV>();
     const int r = warp / 4, quarter = warp % 4;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t st_t = tmem + lane_off + 128 * r, dpt_t = st_t + BH2;
@@ -430,22 +468,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n_ne;
       tc_fence_after();
       const float mul = r == 0 ? 1.0f : p.scale;
-      __nv_bfloat16* grow = grad_row();
+      // the warp's 32 keys' rows, 64 bytes (32 columns) at a time
+      uint8_t* wbase = reinterpret_cast<uint8_t*>(grad_row() - lane * D);
+      const int live_keys = p.Sk - (j * BT + quarter * 32);
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
-        uint32_t a[32];
+        uint32_t a[32], w[16];
         tmem_ld32_wait(acc_t + 32 * cb, a);
-        if (key_live) {
-          uint4* d4 = reinterpret_cast<uint4*>(grow + 32 * cb);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t w[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h)
-              w[h] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * h]) * mul, __uint_as_float(a[8 * q4 + 2 * h + 1]) * mul);
-            d4[q4] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        }
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * mul, __uint_as_float(a[2 * e + 1]) * mul);
+        store_warp_rows<4>(w, wbase + 64 * cb, 2 * D, live_keys, lane);
       }
       tc_fence_before();
       mbar_arrive(&acc_empty);  // dV and dK may be overwritten by the next item
@@ -740,22 +773,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++t;
       tc_fence_after();
+      // the warp's 32 rows, this warpgroup's D/2 columns (D bytes) of each
+      {
+        constexpr int CH = D / 16;
+        uint32_t w[4 * CH];
 #pragma unroll
-      for (int cb = 0; cb < D / 64; ++cb) {
-        uint32_t a[32];
-        tmem_ld32_wait(dq_t + r * (D / 2) + 32 * cb, a);
-        if (live) {
-          uint4* d4 = reinterpret_cast<uint4*>(dqrow + 32 * cb);
+        for (int cb = 0; cb < D / 64; ++cb) {
+          uint32_t a[32];
+          tmem_ld32_wait(dq_t + r * (D / 2) + 32 * cb, a);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t w[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h)
-              w[h] = pack_bf16x2(__uint_as_float(a[8 * q4 + 2 * h]) * p.scale,
-                                 __uint_as_float(a[8 * q4 + 2 * h + 1]) * p.scale);
-            d4[q4] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          for (int e = 0; e < 16; ++e)
+            w[16 * cb + e] = pack_bf16x2(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
         }
+        store_warp_rows<CH>(w, reinterpret_cast<uint8_t*>(dqrow - lane * D), 2 * D, p.Sq - (i * BT + quarter * 32),
+                            lane);
       }
       tc_fence_before();
       mbar_arrive(&acc_empty);
