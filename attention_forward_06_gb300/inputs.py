@@ -73,6 +73,18 @@ def draw_workload(w: Workload):
     return draw(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.seed, w.qk_std, w.v_std)
 
 
+def draw_on_device(shape, seed, std=1.0, device="cuda"):
+    """One bf16 tensor of N(0, std^2) entries drawn on ``device`` with a seeded generator, one slice of the
+    second dimension at a time (fp32 normals, scaled, rounded to bf16 nearest-even).  For inputs of several GB,
+    which take too long to draw on the CPU; whoever checks the result copies out the rows it needs."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    for h in range(shape[1]):
+        out[:, h].copy_(torch.randn(out[:, h].shape, generator=g, dtype=torch.float32, device=device) * std)
+    return out
+
+
 def sample_rows(B, Hq, Sq, per_head, seed):
     """Distinct uniformly drawn query rows per (b, h), always including rows 0 and Sq-1.
 
