@@ -49,7 +49,11 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # ATTN_REF_LIB names another build of attn_ref.c to load instead: the mutation test
+            # (tests/test_oracle_mutants.py) runs the pin suites, in a child process, against copies of the
+            # oracle with one planted mistake each, and requires every copy to fail a pin.
+            override = os.environ.get("ATTN_REF_LIB")
+            lib = ctypes.CDLL(override if override else build())
             u16p = ctypes.POINTER(ctypes.c_uint16)
             f64p = ctypes.POINTER(ctypes.c_double)
             i64p = ctypes.POINTER(ctypes.c_int64)
