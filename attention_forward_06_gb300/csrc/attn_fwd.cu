@@ -574,35 +574,90 @@ __global__ void __launch_bounds__(kThreads, 1)
       issue_s(0, kslot, smem_u32(&s_full[0]));
       issue_s(1, kslot, smem_u32(&s_full[1]), smem_u32(&kv_empty[kslot]));
       if (n == 1) mma_commit_elect(&q_empty);
-      for (int j = 0; j < n; ++j) {
+      // One step: P.V of both Q tiles on V_j and, unless it is the item's last, their S on K_(j+1).
+      // At D = 64, where the softmax sets the pace, the first, second-last and last steps are separate
+      // compile-time variants, so the steady-state step carries no per-step test (2.6 % faster on a chunked
+      // prefill at D = 64; no gain at D = 128, which keeps the plain loop).
+      auto step = [&](auto first_c, auto last_c, auto qlast_c) -> bool {
+        constexpr bool first = decltype(first_c)::value;  // j == 0: the O_t of the previous item must be read out
+        constexpr bool last = decltype(last_c)::value;    // j == n - 1: the P.V complete O_t
+        constexpr bool qlast = decltype(qlast_c)::value;  // j == n - 2: the S issued here are the item's last
         const uint32_t vslot = kv_it % S;
-        ok = wait_kv(kv_it);
+        bool good = wait_kv(kv_it);
         ++kv_it;
-        if (ok && j == 0 && n_done > 0) ok = warp_wait(&o_empty[0], (n_done - 1) & 1, abort_v, kTimeoutNs);
-        if (ok) ok = warp_wait(&p_full[0], g & 1, abort_v, kTimeoutNs);
-        if (!ok) break;
+        if constexpr (first) {
+          if (good && n_done > 0) good = warp_wait(&o_empty[0], (n_done - 1) & 1, abort_v, kTimeoutNs);
+        }
+        if (good) good = warp_wait(&p_full[0], g & 1, abort_v, kTimeoutNs);
+        if (!good) return false;
         tc_fence_after();
         // the last P.V of O_0 completes it: its epilogue can start
-        issue_pv(0, vslot, j > 0, j + 1 == n ? smem_u32(&o_final[0]) : kNoBar);
-        const bool more = j + 1 < n;
-        if (more) {
-          kslot = kv_it % S;
-          ok = wait_kv(kv_it);
+        issue_pv(0, vslot, !first, last ? smem_u32(&o_final[0]) : kNoBar);
+        uint32_t ks = 0;
+        if constexpr (!last) {
+          ks = kv_it % S;
+          good = wait_kv(kv_it);
           ++kv_it;
-          if (!ok) break;
+          if (!good) return false;
           tc_fence_after();
-          issue_s(0, kslot, smem_u32(&s_full[0]));
+          issue_s(0, ks, smem_u32(&s_full[0]));
         }
-        if (j == 0 && n_done > 0) ok = warp_wait(&o_empty[1], (n_done - 1) & 1, abort_v, kTimeoutNs);
-        if (ok) ok = warp_wait(&p_full[1], g & 1, abort_v, kTimeoutNs);
-        if (!ok) break;
+        if constexpr (first) {
+          if (n_done > 0) good = warp_wait(&o_empty[1], (n_done - 1) & 1, abort_v, kTimeoutNs);
+        }
+        if (good) good = warp_wait(&p_full[1], g & 1, abort_v, kTimeoutNs);
+        if (!good) return false;
         tc_fence_after();
-        issue_pv(1, vslot, j > 0, j + 1 == n ? smem_u32(&o_final[1]) : kNoBar, smem_u32(&kv_empty[vslot]));
-        if (more) {
-          issue_s(1, kslot, smem_u32(&s_full[1]), smem_u32(&kv_empty[kslot]));
-          if (j + 2 == n) mma_commit_elect(&q_empty);  // that was the item's last S
+        issue_pv(1, vslot, !first, last ? smem_u32(&o_final[1]) : kNoBar, smem_u32(&kv_empty[vslot]));
+        if constexpr (!last) {
+          issue_s(1, ks, smem_u32(&s_full[1]), smem_u32(&kv_empty[ks]));
+          if constexpr (qlast) mma_commit_elect(&q_empty);  // that was the item's last S
         }
         ++g;
+        return true;
+      };
+      if constexpr (D == 64) {
+        using T = std::true_type;
+        using F = std::false_type;
+        if (n == 1) {
+          ok = step(T{}, T{}, F{});
+        } else {
+          ok = (n == 2) ? step(T{}, F{}, T{}) : step(T{}, F{}, F{});
+          for (int j = 1; ok && j + 2 < n; ++j) ok = step(F{}, F{}, F{});
+          if (ok && n >= 3) ok = step(F{}, F{}, T{});
+          if (ok) ok = step(F{}, T{}, F{});
+        }
+      } else {
+        for (int j = 0; j < n; ++j) {
+          const uint32_t vslot = kv_it % S;
+          ok = wait_kv(kv_it);
+          ++kv_it;
+          if (ok && j == 0 && n_done > 0) ok = warp_wait(&o_empty[0], (n_done - 1) & 1, abort_v, kTimeoutNs);
+          if (ok) ok = warp_wait(&p_full[0], g & 1, abort_v, kTimeoutNs);
+          if (!ok) break;
+          tc_fence_after();
+          // the last P.V of O_0 completes it: its epilogue can start
+          issue_pv(0, vslot, j > 0, j + 1 == n ? smem_u32(&o_final[0]) : kNoBar);
+          const bool more = j + 1 < n;
+          if (more) {
+            kslot = kv_it % S;
+            ok = wait_kv(kv_it);
+            ++kv_it;
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(0, kslot, smem_u32(&s_full[0]));
+          }
+          if (j == 0 && n_done > 0) ok = warp_wait(&o_empty[1], (n_done - 1) & 1, abort_v, kTimeoutNs);
+          if (ok) ok = warp_wait(&p_full[1], g & 1, abort_v, kTimeoutNs);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, vslot, j > 0, j + 1 == n ? smem_u32(&o_final[1]) : kNoBar, smem_u32(&kv_empty[vslot]));
+          if (more) {
+            issue_s(1, kslot, smem_u32(&s_full[1]), smem_u32(&kv_empty[kslot]));
+            if (j + 2 == n) mma_commit_elect(&q_empty);  // that was the item's last S
+          }
+          ++g;
+        }
       }
       if (!ok) break;
       ++n_done;
