@@ -585,6 +585,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vslot = kv_it % S;
         bool good = wait_kv(kv_it);
         ++kv_it;
+        // K_(j+1) is awaited here, before the softmax hand-off, not between P.V_0 and S_0 (its ring slot
+        // was released steps ago, so the wait does not depend on this step's products)
+        uint32_t ks = 0;
+        if constexpr (!last) {
+          ks = kv_it % S;
+          if (good) good = wait_kv(kv_it);
+          ++kv_it;
+        }
         if constexpr (first) {
           if (good && n_done > 0) good = warp_wait(&o_empty[0], (n_done - 1) & 1, abort_v, kTimeoutNs);
         }
@@ -593,15 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // the last P.V of O_0 completes it: its epilogue can start
         issue_pv(0, vslot, !first, last ? smem_u32(&o_final[0]) : kNoBar);
-        uint32_t ks = 0;
-        if constexpr (!last) {
-          ks = kv_it % S;
-          good = wait_kv(kv_it);
-          ++kv_it;
-          if (!good) return false;
-          tc_fence_after();
-          issue_s(0, ks, smem_u32(&s_full[0]));
-        }
+        if constexpr (!last) issue_s(0, ks, smem_u32(&s_full[0]));
         if constexpr (first) {
           if (n_done > 0) good = warp_wait(&o_empty[1], (n_done - 1) & 1, abort_v, kTimeoutNs);
         }
