@@ -64,7 +64,8 @@ def conv_flops(w: Workload) -> float:
 
 
 def min_hbm_bytes(w: Workload) -> int:
-    return 2 * w.B * (w.Hq * w.Sq * w.D * 2 + w.Hkv * w.Sk * w.D) + 4 * w.B * w.Hq * w.Sq
+    """Bytes of Q, K, V, O (bf16) and LSE (fp32), each moved once."""
+    return 2 * (2 * w.B * w.Hq * w.Sq * w.D + 2 * w.B * w.Hkv * w.Sk * w.D) + 4 * w.B * w.Hq * w.Sq
 
 
 def blocksparse_pairs(w: Workload, blocks: np.ndarray, block: int = 128) -> int:
