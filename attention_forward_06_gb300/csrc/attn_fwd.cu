@@ -28,19 +28,31 @@
 // have read O out of TMEM (o_empty), and the next item's Q only waits for the
 // last S of this one (q_empty).
 // TMEM columns: S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [384,384+D); P_t
-// (bf16 pairs) overwrites the last 64 columns of S_t once S_t is in registers,
+// (fp16 pairs) overwrites the last 64 columns of S_t once S_t is in registers,
 // so the S of the first 64 keys stays readable until the next S_t.
 //
+// P.V runs in fp16: P is rounded to fp16 (11 significant bits against bf16's 8,
+// which keeps the rounding of P four times smaller) and each V tile is converted
+// to fp16 in place in its ring slot before its product, by the softmax warps
+// between one tile's hand-off and the next tile's S (exact for |v| in [2^-14,
+// 65504]; smaller magnitudes round to fp16's subnormal grid, larger ones become
+// infinite).
+//
 // Online softmax per row, in log2 units (c = scale * log2 e), with a lazy
-// running max m: a tile's exponentials are taken against the current m, and
-// the tile's row max is only computed (and m raised, when it exceeds m by more
-// than 8) on a row's first tile or when the tile's P mass under the stale m
-// exceeds 2^32.  Any m is exact because O and the normalisers share it.  l sums
-// the bf16-rounded P values the tensor cores multiply (taken after P has been
-// handed to the MMA), so the final O / l is a convex combination of V rows; a
-// second, fp32 sum of the unrounded P gives the LSE.  Causal masking touches
-// only the tiles that straddle the diagonal (or the ragged end of K); tiles
-// wholly above the diagonal are never loaded.
+// reference value m: a tile's exponentials are taken against the current m,
+// and the tile's row max is only computed on a row's first tile (or while it
+// has seen no key), where m is set 8 above it, so P starts at most 2^-8 and a
+// later key may exceed that first max by up to 2^24 before P leaves fp16's
+// range.  When a tile's P mass does pass fp16's largest value 65504 (the rare
+// case), m moves up by the power of two that brings the mass below 2^-8 (keys
+// 0-63 scale their fp32 P, keys 64-127 redo theirs from S), or, for a mass
+// beyond 2^64 or not finite, to 8 above the tile's row max.  Any m gives the
+// exact result because O and both normalisers share it.  l sums the
+// fp16-rounded P values the tensor cores multiply (taken after P has been handed
+// to the MMA), so the final O / l is a convex combination of V rows; a second,
+// fp32 sum of the unrounded P gives the LSE.  Causal masking touches only the
+// tiles that straddle the diagonal (or the ragged end of K); tiles wholly above
+// the diagonal are never loaded.
 //
 // Every mbarrier wait is bounded: a wait that runs out sets a shared abort
 // flag and a device status word, and all roles unwind to the final barrier,
@@ -79,8 +91,10 @@ static_assert(128 * kRegsOther + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s per wait
 constexpr uint64_t kDrainTimeoutNs = 500000000ull;
-constexpr float kRescaleThreshold = 8.0f;       // log2 units
-constexpr float kLazyMassLimit = 4294967296.0f; // largest tile P mass accepted without a row max (2^32)
+constexpr float kHeadroom = 8.0f;       // log2 units: m is set this far above a tile's row max
+constexpr int kHeadroomBits = 8;
+constexpr float kF16Max = 65504.0f;     // largest finite fp16: a tile's P mass above it may overflow
+constexpr float kScaleMassLimit = 18446744073709551616.0f;  // 2^64: beyond it a tile is redone from S
 
 // Sites recorded in the device status word when a wait runs out.
 constexpr int kSiteProducer = 1;
@@ -101,7 +115,7 @@ struct Cfg {
   // next to O (TMEM has room for it only at D = 64).
   static constexpr bool kTensorRowSum = (D == 64);
   static constexpr int kPvN = kTensorRowSum ? D + 16 : D;  // MMA N of the P.V product
-  static constexpr int kOnesBytes = kTensorRowSum ? BN * 128 : 0;  // 128 keys x 64 columns of bf16 1.0
+  static constexpr int kOnesBytes = kTensorRowSum ? BN * 128 : 0;  // 128 keys x 64 columns of fp16 1.0
   static constexpr int kSmemBytes =
       kQBytes + kStages * kTileBytes + kStageBufs * kStageBytes + kOnesBytes + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -344,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* st_s = kv_s + S * C::kTileBytes;  // O staging buffer b at st_s + b * kStageBytes
   uint8_t* ones_s = st_s + C::kStageBufs * C::kStageBytes;  // D = 64: the ones block of the row-sum columns
   __shared__ uint64_t kv_full[S], kv_empty[S];
+  __shared__ uint64_t v_ready[S];  // a V tile in slot s has been converted to fp16 (odd slots only)
   __shared__ uint64_t q_full, q_empty, s_full[QTILES], p_full[QTILES], o_final[QTILES], o_empty[QTILES];
   __shared__ uint64_t stage_full[QTILES], stage_rel[QTILES], mma_drain;
   __shared__ uint64_t seq_full[kSeqSlots], seq_empty[kSeqSlots];
@@ -359,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
+      mbar_init(&v_ready[s], 8);  // one arrival per softmax warp
     }
     mbar_init(&q_full, 1);
     mbar_init(&q_empty, 1);
@@ -383,10 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if constexpr (C::kTensorRowSum) {
-    // bf16 1.0 everywhere (the swizzle does not matter for a constant block), made
+    // fp16 1.0 everywhere (the swizzle does not matter for a constant block), made
     // visible to the tensor cores' (async proxy) reads
     for (int i = threadIdx.x; i < C::kOnesBytes / 16; i += kThreads)
-      reinterpret_cast<uint4*>(ones_s)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+      reinterpret_cast<uint4*>(ones_s)[i] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -525,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tcgen05 issuer
     const uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
-    const uint32_t idesc_pv = idesc_bf16_f32(BM, C::kPvN, true);
+    const uint32_t idesc_pv = idesc_f16_f32(BM, C::kPvN, true);  // fp16 P (TMEM) times fp16 V (smem)
     const uint32_t q_addr = smem_u32(q_s);
     const uint32_t kv_addr = smem_u32(kv_s);
     // The whole warp runs the issue code (converged); one elected lane issues.
@@ -551,9 +567,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       static_assert(BN == 128, "K steps of mma_bf16_ts_k8");
       mma_bf16_ts_k8(tmem + 2 * BN + t * 128, tmem + t * BN + 64, vd, idesc_pv, accumulate ? 1u : 0u, bar0, bar1);
     };
-    // wait for load number `n` of the K/V stream
+    // wait for load number `n` of the K/V stream (a K tile), or for its conversion (a V tile)
     auto wait_kv = [&](uint32_t n) {
       return warp_wait(&kv_full[n % S], (n / S) & 1, abort_v, kTimeoutNs);
+    };
+    auto wait_v = [&](uint32_t n) {
+      return warp_wait(&v_ready[n % S], (n / S) & 1, abort_v, kTimeoutNs);
     };
     uint32_t kv_it = 0;   // K/V loads consumed
     uint32_t g = 0;       // key tiles processed over all items (p_full phase)
@@ -584,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr bool last = decltype(last_c)::value;    // j == n - 1: the P.V complete O_t
         constexpr bool qlast = decltype(qlast_c)::value;  // j == n - 2: the S issued here are the item's last
         const uint32_t vslot = kv_it % S;
-        bool good = wait_kv(kv_it);
+        bool good = wait_v(kv_it);
         ++kv_it;
         // K_(j+1) is awaited here, before the softmax hand-off, not between P.V_0 and S_0 (its ring slot
         // was released steps ago, so the wait does not depend on this step's products)
@@ -631,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         for (int j = 0; j < n; ++j) {
           const uint32_t vslot = kv_it % S;
-          ok = wait_kv(kv_it);
+          ok = wait_v(kv_it);
           ++kv_it;
           if (ok && j == 0 && n_done > 0) ok = warp_wait(&o_empty[0], (n_done - 1) & 1, abort_v, kTimeoutNs);
           if (ok) ok = warp_wait(&p_full[0], g & 1, abort_v, kTimeoutNs);
@@ -752,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         lim_tile = min(lim_tile, tile_row0 + p.diag);
       }
       float m = -INFINITY;   // running max, log2 units
-      float l = 0.0f;        // sum of the bf16-rounded P the tensor cores use (normalises O)
+      float l = 0.0f;        // sum of the fp16-rounded P the tensor cores use (normalises O)
       float l_exact = 0.0f;  // sum of the fp32 P (gives LSE)
 
       // block-sparse mode: walk the same marked tiles as the producer; a tile that only
@@ -787,6 +806,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the tile is unmarked for this Q tile, or straddles the diagonal or the end of K
         const bool masked = !own || jg * BN + BN - 1 > lim_tile;
         const int kmax = own ? lim - jg * BN : -1;
+        // V of this tile (load 2g + 1 of the CTA's K/V stream) to fp16, in place in its ring
+        // slot: the 256 softmax threads take one 16-byte chunk in 256 each (a chunk holds 8
+        // consecutive values of one row, so the swizzled layout is unchanged), make their
+        // writes visible to the tensor cores and arrive on v_ready.  This runs between the
+        // previous tile's hand-off and the wait for this tile's S, while the tensor cores
+        // work on the P.V and S products issued in between; the slot is refilled only after
+        // the P.V that waited for v_ready has read it.
+        {
+          const uint32_t vn = 2u * g + 1u;
+          ok = warp_wait(&kv_full[vn % S], (vn / S) & 1, abort_v, kTimeoutNs);
+          if (!ok) break;
+          constexpr int kChunks = C::kTileBytes / 16 / 256;  // per thread: 8 (D = 128) or 4 (D = 64)
+          const uint32_t base = smem_u32(kv_s + (vn % S) * C::kTileBytes) + 16u * threadIdx.x;
+          uint4 w[kChunks];
+#pragma unroll
+          for (int u = 0; u < kChunks; ++u) w[u] = lds128(base + 4096u * u);
+#pragma unroll
+          for (int u = 0; u < kChunks; ++u) {
+            w[u].x = bf16x2_to_f16x2(w[u].x);
+            w[u].y = bf16x2_to_f16x2(w[u].y);
+            w[u].z = bf16x2_to_f16x2(w[u].z);
+            w[u].w = bf16x2_to_f16x2(w[u].w);
+            sts128(base + 4096u * u, w[u]);
+          }
+          fence_proxy_async_smem();  // this thread's writes are visible to the tensor cores' reads
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&v_ready[vn % S]);
+        }
         ok = warp_wait(&s_full[t], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
@@ -812,9 +859,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 128; ++i) r[i] = (i > kmax) ? __float_as_uint(-INFINITY) : r[i];
         }
-        // Row max of the tile; raises m (and rescales l, l_exact and O_t) when the
-        // tile's max exceeds it by more than kRescaleThreshold.
-        auto row_max = [&]() {
+        const float m_in = m;  // the reference value the tile starts from
+        // Row max of the tile; when it exceeds m, m moves kHeadroom above it.
+        auto raise_to_tile_max = [&]() {
           float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
           for (int i = 0; i < 128; i += 8) {
@@ -824,16 +871,132 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx3 = max3f(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
           }
           const float m_tile = fmaxf(max3f(mx0, mx1, mx2), mx3) * c;
-          const bool raise = m_tile > m + kRescaleThreshold;
-          float alpha = 1.0f;
-          if (raise) {
-            alpha = ex2_approx(m - m_tile);
-            m = m_tile;
-            l *= alpha;
-            l_exact *= alpha;
+          if (m_tile > m) m = m_tile + kHeadroom;
+        };
+        // P = exp2(s * c - m): packed FMA and one ex2 per element, fp16 pairs into TMEM
+        // columns 64-127 of S_t (P over keys 0-63, then 64-127), and the fp32 sum of P.
+        // Keys 0-63 keep their fp32 P in r (in place of S); keys 64-127 keep their S in r.
+        // The S of keys 0-63 also stays in TMEM columns 0-63 until the next S_t.
+        uint64_t le0, le1;
+        uint32_t pk0[32], pk1[32];
+        auto exp_lo = [&]() {
+          const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+          const uint64_t c2 = f2_pack(c, c);
+          const uint64_t nm2 = f2_pack(neg_m, neg_m);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float x0, x1;
+            f2_unpack(ffma2(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c2, nm2), x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            r[2 * i] = __float_as_uint(p0);
+            r[2 * i + 1] = __float_as_uint(p1);
+            pk0[i] = pack_f16x2(p0, p1);
+            if (i & 1)
+              le1 = fadd2(le1, f2_pack(p0, p1));
+            else
+              le0 = fadd2(le0, f2_pack(p0, p1));
           }
-          if (j > 0 && __any_sync(0xffffffffu, raise)) {
-            // rescale this warp's 32 rows of O_t (PV_t(j-1) has completed: its commit preceded S_t(j)'s)
+          tmem_st32(s_tmem + 64, pk0);
+        };
+        auto exp_hi = [&]() {
+          const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+          const uint64_t c2 = f2_pack(c, c);
+          const uint64_t nm2 = f2_pack(neg_m, neg_m);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float x0, x1;
+            f2_unpack(ffma2(f2_pack(__uint_as_float(r[64 + 2 * i]), __uint_as_float(r[64 + 2 * i + 1])), c2, nm2),
+                      x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            pk1[i] = pack_f16x2(p0, p1);
+            if (i & 1)
+              le1 = fadd2(le1, f2_pack(p0, p1));
+            else
+              le0 = fadd2(le0, f2_pack(p0, p1));
+          }
+          tmem_st32(s_tmem + 96, pk1);
+        };
+        auto mass = [&]() {
+          float a0, a1, b0, b1;
+          f2_unpack(le0, a0, a1);
+          f2_unpack(le1, b0, b1);
+          return (a0 + a1) + (b0 + b1);
+        };
+        // The row max only on a row's first tile, or while the row has seen no key.
+        const bool first = __any_sync(0xffffffffu, j == 0 || m == -INFINITY);
+        if (first) raise_to_tile_max();
+        le0 = f2_pack(0.0f, 0.0f);
+        le1 = le0;
+        exp_lo();
+        exp_hi();
+        float tile_le = mass();
+        // Rare: the tile's P mass passes fp16's largest value (NaN fails the comparison
+        // too), so some P may have overflowed in fp16.  A finite mass up to 2^64 moves m
+        // up by the exponent that brings it below 2^-8: keys 0-63 scale their fp32 P by
+        // that power of two (exact), keys 64-127 redo theirs from S.  A larger or
+        // non-finite mass takes the row max instead, with the S of keys 0-63 reloaded
+        // from TMEM.  Both halves of P are then stored again.
+        const bool slow = __any_sync(0xffffffffu, !(tile_le <= kF16Max));
+        if (slow) {
+          float sc = 1.0f;
+          const bool huge = !(tile_le <= kScaleMassLimit);
+          if (!(tile_le <= kF16Max) && !huge) {
+            const int e = (__float_as_int(tile_le) >> 23) - 127;  // mass in [2^e, 2^(e+1)), e >= 15
+            const int shift = e + 1 + kHeadroomBits;
+            sc = __int_as_float((127 - shift) << 23);
+            m += static_cast<float>(shift);
+          }
+          tmem_wait_st();  // the first pass's P stores have landed before they are overwritten
+          if (__any_sync(0xffffffffu, huge)) {
+            uint32_t s0[32], s1[32];
+            tmem_ld32_wait(s_tmem, s0);
+            tmem_ld32_wait(s_tmem + 32, s1);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              s0[i] = (masked && i > kmax) ? __float_as_uint(-INFINITY) : s0[i];
+              s1[i] = (masked && 32 + i > kmax) ? __float_as_uint(-INFINITY) : s1[i];
+              mx = max3f(mx, __uint_as_float(s0[i]), __uint_as_float(s1[i]));
+            }
+#pragma unroll
+            for (int i = 64; i < 128; i += 2) mx = max3f(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+            mx *= c;
+            if (huge && mx > m) m = mx + kHeadroom;
+            const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {  // huge rows: P of keys 0-63 again from S
+              const float q0 = ex2_approx(fmaf(__uint_as_float(s0[i]), c, neg_m));
+              const float q1 = ex2_approx(fmaf(__uint_as_float(s1[i]), c, neg_m));
+              r[i] = huge ? __float_as_uint(q0) : r[i];
+              r[32 + i] = huge ? __float_as_uint(q1) : r[32 + i];
+            }
+          }
+          le0 = f2_pack(0.0f, 0.0f);
+          le1 = le0;
+          const uint64_t sc2 = f2_pack(sc, sc);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float p0, p1;
+            f2_unpack(fmul2(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc2), p0, p1);
+            pk0[i] = pack_f16x2(p0, p1);
+            if (i & 1)
+              le1 = fadd2(le1, f2_pack(p0, p1));
+            else
+              le0 = fadd2(le0, f2_pack(p0, p1));
+          }
+          tmem_st32(s_tmem + 64, pk0);
+          exp_hi();
+          tile_le = mass();
+        }
+        // m moved: bring l, l_exact and (past the item's first tile) O_t to the new m.
+        // O_t can be rewritten here: P.V_t(j-1) completed before S_t(j), whose commit came after it.
+        const float alpha = (m == m_in) ? 1.0f : ex2_approx(m_in - m);
+        if ((first || slow) && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          l *= alpha;
+          l_exact *= alpha;
+          if (j > 0) {
             const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
             for (int cb = 0; cb < (C::kPvN + 31) / 32; ++cb) {  // O and, at D = 64, the row-sum columns
@@ -849,85 +1012,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_st32(o_tmem + cb * 32, o);
             }
           }
-        };
-        // P = exp2(s * c - m) for one half of the keys: packed FMA, one ex2 per
-        // element, bf16 pairs into TMEM columns 64-127 of S_t (P over keys 0-63 then
-        // 64-127), and the fp32 sum of P.  The S values of keys 0-63 (TMEM columns
-        // 0-63) stay intact until the next S_t.
-        uint64_t le0, le1;
-        uint32_t pk0[32], pk1[32];
-        auto exp_half = [&](auto half_c, uint32_t(&pk)[32]) {
-          constexpr int half = decltype(half_c)::value;
-          const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-          const uint64_t c2 = f2_pack(c, c);
-          const uint64_t nm2 = f2_pack(neg_m, neg_m);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int e = half * 64 + 2 * i;
-            float x0, x1;
-            f2_unpack(ffma2(f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2), x0, x1);
-            const float p0 = ex2_approx(x0);
-            const float p1 = ex2_approx(x1);
-            pk[i] = pack_bf16x2(p0, p1);
-            if (i & 1)
-              le1 = fadd2(le1, f2_pack(p0, p1));
-            else
-              le0 = fadd2(le0, f2_pack(p0, p1));
-          }
-          tmem_st32(s_tmem + 64 + half * 32, pk);
-        };
-        auto tile_mass = [&]() {
-          float a0, a1, b0, b1;
-          f2_unpack(le0, a0, a1);
-          f2_unpack(le1, b0, b1);
-          return (a0 + a1) + (b0 + b1);
-        };
-        // Lazy row max.  The exponentials are taken against the running max m
-        // first; the row max of the tile is only computed (and m raised) on the
-        // first tile of a row, while a row has seen no key, or when that pass shows
-        // the tile's P mass above kLazyMassLimit.  Any m is exact here: O and both
-        // normalisers share it, and P, l and O keep full relative precision at any
-        // magnitude, so a stale m only costs headroom (P stays below 2^32).
-        const bool first = __any_sync(0xffffffffu, j == 0 || m == -INFINITY);
-        if (first) row_max();
-        le0 = f2_pack(0.0f, 0.0f);
-        le1 = le0;
-        exp_half(std::integral_constant<int, 0>{}, pk0);
-        exp_half(std::integral_constant<int, 1>{}, pk1);
-        float tile_le = tile_mass();
-        // NaN or overflow fails the comparison too
-        if (!first && __any_sync(0xffffffffu, !(tile_le <= kLazyMassLimit))) {
-          // rare: reload the S of keys 0-63 (P now sits over keys 64-127, whose S is
-          // still in registers), take the row max, and redo the exponentials
-          {
-            uint32_t s0[32], s1[32];
-            tmem_ld32_wait(s_tmem, s0);
-            tmem_ld32_wait(s_tmem + 32, s1);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              r[i] = (masked && i > kmax) ? __float_as_uint(-INFINITY) : s0[i];
-              r[32 + i] = (masked && 32 + i > kmax) ? __float_as_uint(-INFINITY) : s1[i];
-            }
-          }
-          row_max();
-          le0 = f2_pack(0.0f, 0.0f);
-          le1 = le0;
-          exp_half(std::integral_constant<int, 0>{}, pk0);
-          exp_half(std::integral_constant<int, 1>{}, pk1);
-          tile_le = tile_mass();
         }
         l_exact += tile_le;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
-        if constexpr (!C::kTensorRowSum) {  // the sum of the bf16-rounded P, after the hand-off
+        if constexpr (!C::kTensorRowSum) {  // the sum of the fp16-rounded P, after the hand-off
           float q0 = 0.0f, q1 = 0.0f, q2 = 0.0f, q3 = 0.0f;
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            add_bf16x2_to_f32(q0, q1, pk0[i]);
-            add_bf16x2_to_f32(q2, q3, pk0[i + 1]);
-            add_bf16x2_to_f32(q0, q1, pk1[i]);
-            add_bf16x2_to_f32(q2, q3, pk1[i + 1]);
+            add_f16x2_to_f32(q0, q1, pk0[i]);
+            add_f16x2_to_f32(q2, q3, pk0[i + 1]);
+            add_f16x2_to_f32(q0, q1, pk1[i]);
+            add_f16x2_to_f32(q2, q3, pk1[i + 1]);
           }
           l += (q0 + q1) + (q2 + q3);
         }

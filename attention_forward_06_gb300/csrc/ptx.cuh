@@ -451,6 +451,13 @@ __device__ __forceinline__ uint32_t opaque(uint32_t x) {
   return x;
 }
 
+// Instruction descriptor, kind::f16 with fp16 A/B and fp32 D: the bf16 one with
+// both operand formats 0 (f16).  A and B always share one type in a kind::f16 MMA.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D:
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
 //   bit 15 A major (0 = K), bit 16 B major (0 = K, 1 = MN), bits 17-22 N>>3, bits 24-28 M>>4.
@@ -646,6 +653,42 @@ __device__ __forceinline__ void add_bf16x2_to_f32(float& acc_lo, float& acc_hi, 
       "add.rn.f32.bf16 %1, hi, %1;\n\t}"
       : "+f"(acc_lo), "+f"(acc_hi)
       : "r"(packed));
+}
+
+// acc_lo += fp16 in bits 0-15 of `packed`, acc_hi += fp16 in bits 16-31 (mixed-precision adds).
+__device__ __forceinline__ void add_f16x2_to_f32(float& acc_lo, float& acc_hi, uint32_t packed) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\t"
+      "add.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(packed));
+}
+
+// Round two fp32 values to fp16 (nearest-even; beyond 65504 gives infinity) and
+// pack: `lo` in bits 0-15, `hi` in 16-31.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// A bf16 pair to the fp16 pair of the same values: exact for magnitudes in
+// [2^-14, 65504], rounded to fp16's subnormal grid below, infinite above.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// 16-byte shared-memory load and store at a shared-window address.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
 }
 
 // Change this warpgroup's per-thread register budget (all four warps execute it).

@@ -38,9 +38,13 @@
  * entry point, per-device capability check and kernel attributes) is guarded.
  *
  * Precision.  bf16 inputs; both products accumulate in fp32 on the tensor
- * cores; softmax in fp32 with exp2; P is rounded to bf16 before the P.V
- * product and the normaliser sums those same rounded values; O is rounded to
- * bf16 (nearest-even) once, at the end.
+ * cores; softmax in fp32 with exp2.  The P.V product runs in fp16: P is rounded
+ * to fp16 (nearest-even) and the normaliser sums those same rounded values, and
+ * each V tile is converted to fp16 inside the kernel (exact for magnitudes in
+ * [2^-14, 65504]; smaller ones round to fp16's subnormal grid, an absolute
+ * error below 2^-25).  V entries beyond 65504 in magnitude are outside the
+ * supported range: they become infinite and make the affected O rows
+ * non-finite.  O is rounded to bf16 (nearest-even) once, at the end.
  */
 #ifndef ATTN_FWD_H
 #define ATTN_FWD_H

@@ -1,23 +1,37 @@
 """Comparison of the CUDA path's outputs with the fp64 oracle's.
 
 Tolerances: |dLSE| <= 1e-3 and |dO| <= 1e-2 (bf16 inputs, fp32 accumulation).
-O leaves the kernel as bf16, and even the best bf16 value -- the exact result
-rounded to nearest -- sits up to half a bf16 spacing from the exact result
-(2^-8 for |O| in [2, 4), 2^-7 in [4, 8): more than 1e-2 there).  So the O
-bound is applied to the error *in excess of that unavoidable rounding*:
 
-    |O_gpu - O_ref| <= |bf16(O_ref) - O_ref| + 1e-2      for every element,
+O leaves the kernel as bf16.  Below 4 in magnitude the bf16 spacing is at most
+2^-6, so some bf16 value lies within 2^-7 (0.0078) of any exact result there,
+and the plain bound applies to every such element:
 
-i.e. the kernel's output is never more than 1e-2 worse than the best possible
-bf16 output.  The plain max |dO| is reported beside it.
+    |O_gpu - O_ref| <= 1e-2                             where |O_ref| < 4.
+
+From 4 upwards the spacing is 2^-5 or more: the exact result rounded to the
+nearest bf16 can sit up to 0.0156 away, so no bf16 output meets 1e-2 on every
+element.  There the bound is applied to the error in excess of that
+unavoidable rounding:
+
+    |O_gpu - O_ref| <= |bf16(O_ref) - O_ref| + 1e-2     where |O_ref| >= 4.
+
+The statistics give the plain max |dO| in bins of |O_ref| ([0,1), [1,2),
+[2,4), [4,8), [8,inf)) beside the maximum excess over the rounding floor.
+When the environment variable ATTN_PARITY_STATS names a file, every comparison
+made with a ``label`` appends its statistics there as one JSON line.
 """
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 import torch
 
 TOL_O = 1e-2
 TOL_LSE = 1e-3
+PLAIN_BELOW = 4.0  # |O_ref| below which the plain bound applies (some bf16 value within 2^-7)
+BINS = ((0.0, 1.0), (1.0, 2.0), (2.0, 4.0), (4.0, 8.0), (8.0, np.inf))
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
@@ -31,23 +45,45 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
     return out
 
 
-def compare(o_gpu: torch.Tensor, lse_gpu: torch.Tensor, o_ref: np.ndarray, lse_ref: np.ndarray) -> dict:
+def o_bound(o_ref: np.ndarray) -> np.ndarray:
+    """Largest |O_gpu - O_ref| accepted per element (see the module docstring)."""
+    a = np.abs(o_ref)
+    floor = np.abs(round_to_bf16(o_ref) - o_ref)
+    return np.where(a < PLAIN_BELOW, TOL_O, floor + TOL_O)
+
+
+def _bin_name(lo, hi):
+    return f"[{lo:g},{hi:g})" if np.isfinite(hi) else f"[{lo:g},inf)"
+
+
+def compare(o_gpu: torch.Tensor, lse_gpu: torch.Tensor, o_ref: np.ndarray, lse_ref: np.ndarray,
+            label: str | None = None) -> dict:
     """Check element by element; return the statistics (raise AssertionError on a violation)."""
     o = o_gpu.detach().cpu().float().numpy().astype(np.float64).reshape(o_ref.shape)
     lse = lse_gpu.detach().cpu().numpy().astype(np.float64).reshape(lse_ref.shape)
     assert np.all(np.isfinite(o)), "non-finite O"
     d = np.abs(o - o_ref)
-    floor = np.abs(round_to_bf16(o_ref) - o_ref)
-    excess = d - floor
+    a = np.abs(o_ref)
+    bound = o_bound(o_ref)
+    big = a >= PLAIN_BELOW
+    excess = d[big] - np.abs(round_to_bf16(o_ref[big]) - o_ref[big])
     stats = {
+        "elements": int(d.size),
         "max_abs_dO": float(d.max()) if d.size else 0.0,
-        "max_excess_dO": float(excess.max()) if d.size else 0.0,
+        "max_abs_dO_below_4": float(d[~big].max()) if np.any(~big) else 0.0,
+        "max_excess_dO_from_4": float(excess.max()) if excess.size else 0.0,
+        "max_abs_dO_by_bin": {},
     }
-    bad = excess > TOL_O
+    for lo, hi in BINS:
+        sel = (a >= lo) & (a < hi)
+        if np.any(sel):
+            stats["max_abs_dO_by_bin"][_bin_name(lo, hi)] = [int(sel.sum()), float(d[sel].max())]
+    bad = d > bound
     if np.any(bad):
-        idx = np.unravel_index(np.argmax(excess), d.shape)
-        raise AssertionError(f"O mismatch at {idx}: gpu {o[idx]} ref {o_ref[idx]} (excess {excess[idx]:.4g} over the "
-                             f"bf16 rounding floor; {int(bad.sum())} of {bad.size} elements out of bound)")
+        idx = np.unravel_index(np.argmax(d - bound), d.shape)
+        raise AssertionError(
+            f"O mismatch at {idx}: gpu {o[idx]} ref {o_ref[idx]} (|dO| {d[idx]:.4g} > bound {bound[idx]:.4g}; "
+            f"{int(bad.sum())} of {bad.size} elements out of bound; per-bin max {stats['max_abs_dO_by_bin']})")
     dead = np.isneginf(lse_ref)
     assert np.all(np.isneginf(lse[dead])), "rows without keys must have LSE = -inf"
     assert np.all(np.isfinite(lse[~dead])), "non-finite LSE on a row with keys"
@@ -55,4 +91,10 @@ def compare(o_gpu: torch.Tensor, lse_gpu: torch.Tensor, o_ref: np.ndarray, lse_r
     dl = np.abs(lse[~dead] - lse_ref[~dead])
     stats["max_abs_dLSE"] = float(dl.max()) if dl.size else 0.0
     assert stats["max_abs_dLSE"] <= TOL_LSE, f"LSE mismatch: {stats['max_abs_dLSE']}"
+    if label is not None:
+        path = os.environ.get("ATTN_PARITY_STATS")
+        if path:
+            with open(path, "a") as f:
+                f.write(json.dumps({"case": label, **stats}) + "\n")
+        print(f"{label}: {json.dumps(stats)}")
     return stats

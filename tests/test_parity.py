@@ -1,7 +1,8 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle, element by
 element on the same seeded inputs: small shapes that span several tiles and
 ragged tails, the edge cases (fully masked rows, one row, one key, no keys,
-grouped heads), and every benchmark workload at full size on sampled rows.
+grouped heads), and every benchmark workload at full size: every row of tiny, train, gqa and both
+chunked shapes, and 256 seeded rows per head of the long-context one.
 """
 import numpy as np
 import pytest
@@ -22,12 +23,12 @@ def run_gpu(q, k, v, causal, scale):
     return o.cpu(), lse.cpu()
 
 
-def full_check(B, Hq, Hkv, Sq, Sk, D, causal, seed, qk_std=1.0):
+def full_check(B, Hq, Hkv, Sq, Sk, D, causal, seed, qk_std=1.0, label=None):
     q, k, v = draw(B, Hq, Hkv, Sq, Sk, D, seed, qk_std=qk_std)
     scale = float(np.float32(D ** -0.5))
     o, lse = run_gpu(q, k, v, causal, scale)
     o_ref, lse_ref = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal, scale)
-    return compare(o, lse, o_ref, lse_ref)
+    return compare(o, lse, o_ref, lse_ref, label=label)
 
 
 SHAPES = [
@@ -58,7 +59,7 @@ def test_small_shapes_match_oracle(shape):
 
 def test_tiny_workload_matches_oracle():
     w = WORKLOADS["tiny"]
-    stats = full_check(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.causal, w.seed)
+    stats = full_check(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.causal, w.seed, label="tiny (all rows)")
     assert stats["max_abs_dO"] <= 1e-2
 
 
@@ -69,14 +70,17 @@ def test_sharp_logits_online_rescale():
 
 
 @pytest.mark.parametrize("Sq,Sk,D,causal,boost", [
-    (256, 512, 128, 0, 20.0),    # a later key tile ~70 log2 units above the first: P mass far above 2^32
+    (256, 512, 128, 0, 20.0),    # a later key tile ~70 log2 units above the first: P mass beyond 2^64 (row max path)
     (384, 384, 64, 1, 100.0),    # first pass overflows to inf; the boosted tile is the diagonal (masked) one
-    (300, 700, 128, 1, 11.0),    # bottom-right, ragged; only part of the rows cross the limit, the rest keep P near 2^30
+    (300, 700, 128, 1, 11.0),    # bottom-right, ragged: masses between 2^16 and 2^64 (power-of-two rescale path)
+    (256, 512, 64, 0, 16.0),     # rows of one warp on both paths at once
 ])
 def test_lazy_max_second_pass(Sq, Sk, D, causal, boost):
-    # The kernel takes a tile's exponentials against the running max first and
-    # recomputes them with the tile's row max when the P mass exceeds 2^32; keys
-    # 256-383 (the third key tile) are scaled so that later tile dominates.
+    # The kernel takes a tile's exponentials against a reference value set 8 above
+    # the first tile's row max; when a later tile's P mass passes fp16's range it
+    # moves the reference up (by a power of two, or to the tile's row max for a mass
+    # beyond 2^64) and stores that tile's P again.  Keys 256-383 (the third key tile)
+    # are scaled so that this later tile dominates.
     q, k, v = draw(1, 4, 2, Sq, Sk, D, seed=int(boost) + Sq)
     k = k.clone()
     k[:, :, 256:384] = (k[:, :, 256:384].float() * boost).to(torch.bfloat16)
@@ -88,19 +92,33 @@ def test_lazy_max_second_pass(Sq, Sk, D, causal, boost):
 
 def test_train_workload_full_oracle():
     w = WORKLOADS["train"]
-    full_check(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, w.causal, w.seed, w.qk_std)
+    q, k, v = draw_workload(w)
+    o, lse = run_gpu(q, k, v, w.causal, w.scale)
+    o_ref, lse_ref = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), w.causal, w.scale)
+    compare(o, lse, o_ref, lse_ref, label="train (all rows)")
 
 
-@pytest.mark.parametrize("name,per_head", [("gqa", 24), ("chunked128", 8), ("chunked64", 8), ("long", 12)])
-def test_full_size_workloads_on_sampled_rows(name, per_head):
+@pytest.mark.parametrize("name", ["gqa", "chunked128", "chunked64"])
+def test_full_size_workloads_every_row(name):
+    # the whole workload against the oracle: every row of every head
     w = WORKLOADS[name]
     q, k, v = draw_workload(w)
     o, lse = run_gpu(q, k, v, w.causal, w.scale)
-    rows = sample_rows(w.B, w.Hq, w.Sq, per_head, seed=w.seed + 1000)
+    o_ref, lse_ref = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), w.causal, w.scale)
+    compare(o, lse, o_ref, lse_ref, label=f"{name} (all rows)")
+
+
+def test_long_context_on_256_rows_per_head():
+    # 256 seeded rows per head (rows 0 and Sq - 1 always among them), 8192 rows in all
+    w = WORKLOADS["long"]
+    q, k, v = draw_workload(w)
+    o, lse = run_gpu(q, k, v, w.causal, w.scale)
+    rows = sample_rows(w.B, w.Hq, w.Sq, 256, seed=w.seed + 1000)
+    assert rows.size == w.B * w.Hq * 256
     o_ref, lse_ref = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), w.causal, w.scale, rows=rows)
     o_rows = o.reshape(-1, w.D)[torch.from_numpy(rows)]
     lse_rows = lse.reshape(-1)[torch.from_numpy(rows)]
-    compare(o_rows, lse_rows, o_ref, lse_ref)
+    compare(o_rows, lse_rows, o_ref, lse_ref, label="long (256 rows per head)")
 
 
 def test_deterministic_bitwise():

@@ -25,7 +25,7 @@ def test_compare_accepts_best_rounding_and_rejects_planted_error():
     lse_ref = rng.normal(size=(2, 3, 5))
     o_best = torch.from_numpy(round_to_bf16(o_ref)).to(torch.bfloat16)
     stats = compare(o_best, torch.from_numpy(lse_ref).float(), o_ref, lse_ref)
-    assert stats["max_excess_dO"] <= 1e-12
+    assert stats["max_excess_dO_from_4"] <= 1e-12 and stats["max_abs_dO_below_4"] <= 2 ** -7
     bad = o_ref.copy()
     bad[1, 2, 3, 4] += 0.05
     with pytest.raises(AssertionError):
@@ -41,3 +41,30 @@ def test_compare_requires_zero_rows_and_minus_inf_where_no_keys():
     compare(good, torch.tensor([[[-float("inf"), 0.5]]]), o_ref, lse_ref)
     with pytest.raises(AssertionError):
         compare(good, torch.tensor([[[0.0, 0.5]]]), o_ref, lse_ref)
+
+
+def test_plain_bound_below_4_and_floor_allowance_from_4():
+    lse_ref = np.zeros((1, 1, 1))
+    lse = torch.zeros((1, 1, 1))
+    # |O_ref| < 4: the next bf16 value up is 0.0101 away -> over the plain 1e-2 bound (the rounding
+    # floor there is 0.0055, so an allowance over the floor would have let it through)
+    o_ref = np.array([[[[3.0 + 0.0055]]]])
+    with pytest.raises(AssertionError):
+        compare(torch.tensor([[[[3.015625]]]]).to(torch.bfloat16), lse, o_ref, lse_ref)
+    stats = compare(torch.tensor([[[[3.0]]]]).to(torch.bfloat16), lse, o_ref, lse_ref)
+    assert abs(stats["max_abs_dO_by_bin"]["[2,4)"][1] - 0.0055) < 1e-12
+    # |O_ref| >= 4: no bf16 value is within 1e-2 of 5.012 (floor 0.012), so one spacing up (0.0193 away)
+    # passes as 0.0073 over the floor; two spacings up (0.0505 away) do not
+    o_ref = np.array([[[[5.0 + 0.012]]]])
+    stats = compare(torch.tensor([[[[5.03125]]]]).to(torch.bfloat16), lse, o_ref, lse_ref)
+    assert abs(stats["max_excess_dO_from_4"] - (0.01925 - 0.012)) < 1e-12
+    with pytest.raises(AssertionError):
+        compare(torch.tensor([[[[5.0625]]]]).to(torch.bfloat16), lse, o_ref, lse_ref)
+
+
+def test_statistics_are_binned_by_reference_magnitude():
+    o_ref = np.array([0.5, 1.5, 3.0, 6.0, 10.0]).reshape(1, 1, 5, 1)
+    o = torch.from_numpy(round_to_bf16(o_ref)).to(torch.bfloat16)
+    stats = compare(o, torch.zeros(1, 1, 5), o_ref, np.zeros((1, 1, 5)))
+    assert sorted(stats["max_abs_dO_by_bin"]) == sorted(["[0,1)", "[1,2)", "[2,4)", "[4,8)", "[8,inf)"])
+    assert all(n == 1 and dmax == 0.0 for n, dmax in stats["max_abs_dO_by_bin"].values())
