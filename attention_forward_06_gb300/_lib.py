@@ -16,7 +16,8 @@ _libs: dict[str, ctypes.CDLL] = {}
 
 _c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
 
-# name -> (restype, argtypes), mirroring include/attn_fwd.h, include/attn_bwd.h and include/attn_fwd_probe.h
+# name -> (restype, argtypes), mirroring include/attn_fwd.h, include/attn_fwd_trace.h, include/attn_bwd.h and
+# include/attn_fwd_probe.h
 SIGNATURES = {
     "attn_fwd": {
         "attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
@@ -33,6 +34,7 @@ SIGNATURES = {
         "attn_fwd_ordered": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp, _c_int, _vp]),
         "attn_fwd_tile_order_entries": (ctypes.c_size_t, [_c_int] * 4),
     },
+    "attn_fwd_trace": {},  # filled below: attn_fwd's entry points and the trace reader
     "attn_bwd": {
         "attn_bwd": (_c_int, [_vp] * 9 + [_c_int] * 7 + [_c_float, _vp, ctypes.c_size_t, _vp]),
         "attn_bwd_workspace_size": (ctypes.c_size_t, [_c_int] * 3),
@@ -43,8 +45,15 @@ SIGNATURES = {
         "attn_probe_mma_ss": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _vp, _vp]),
         "attn_probe_mma_ts": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
         "attn_probe_wait_timeout": (_c_int, [ctypes.c_ulonglong, ctypes.c_ulonglong, _vp, _vp, _vp]),
+        "attn_probe_mma_rate": (_c_int, [_c_int, _c_int, _c_int, _vp, _vp, _vp, _vp]),
+        "attn_probe_ex2_rate": (_c_int, [_c_int, _c_int, _vp, _vp, _vp]),
     },
 }
+
+
+SIGNATURES["attn_fwd_trace"] = dict(SIGNATURES["attn_fwd"])
+SIGNATURES["attn_fwd_trace"]["attn_fwd_trace_read"] = (
+    _c_int, [_vp, ctypes.c_size_t, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)])
 
 
 class LibraryMissing(RuntimeError):

@@ -1,8 +1,9 @@
 """Build the CUDA libraries in-tree with nvcc (sm_103a only).
 
-    libattn_fwd.so    the attention forward pass (C ABI: include/attn_fwd.h)
-    libattn_bwd.so    its backward (C ABI: include/attn_bwd.h)
-    libattn_probe.so  primitive checks of their building blocks (include/attn_fwd_probe.h)
+    libattn_fwd.so        the attention forward pass (C ABI: include/attn_fwd.h)
+    libattn_fwd_trace.so  the same with the kernel's timeline recorded (-DATTN_TRACE; include/attn_fwd_trace.h)
+    libattn_bwd.so        its backward (C ABI: include/attn_bwd.h)
+    libattn_probe.so      primitive checks of their building blocks (include/attn_fwd_probe.h)
 
 The translation units compile in parallel; a library is rebuilt only when a
 source or header is newer than it.  Usage: ``python -m attention_forward_06_gb300.build``.
@@ -28,10 +29,11 @@ NVCC_FLAGS = ARCH + [
     "-cudart", "shared", "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC,
 ]
 
-LIBS = {
-    "attn_fwd": os.path.join(CSRC, "attn_fwd.cu"),
-    "attn_bwd": os.path.join(CSRC, "attn_bwd.cu"),
-    "attn_probe": os.path.join(CSRC, "probe.cu"),
+LIBS = {  # name -> (source, extra nvcc flags)
+    "attn_fwd": (os.path.join(CSRC, "attn_fwd.cu"), []),
+    "attn_fwd_trace": (os.path.join(CSRC, "attn_fwd.cu"), ["-DATTN_TRACE"]),
+    "attn_bwd": (os.path.join(CSRC, "attn_bwd.cu"), []),
+    "attn_probe": (os.path.join(CSRC, "probe.cu"), []),
 }
 
 
@@ -58,10 +60,10 @@ def _stale(name: str) -> bool:
     return any(os.path.getmtime(d) > t for d in _deps())
 
 
-def _compile(name: str, src: str) -> tuple[str, str]:
+def _compile(name: str, src: str, extra: list[str]) -> tuple[str, str]:
     out = lib_path(name)
     tmp = out + f".tmp{os.getpid()}"
-    cmd = [nvcc()] + NVCC_FLAGS + [src, "-o", tmp]
+    cmd = [nvcc()] + NVCC_FLAGS + extra + [src, "-o", tmp]
     proc = subprocess.run(cmd, capture_output=True, text=True)
     log = proc.stdout + proc.stderr
     with open(os.path.join(BUILD_DIR, f"{name}.ptxas.log"), "w") as f:
@@ -78,7 +80,7 @@ def build(force: bool = False, verbose: bool = False) -> dict[str, str]:
     todo = {n: s for n, s in LIBS.items() if force or _stale(n)}
     if todo:
         with ThreadPoolExecutor(max_workers=len(todo)) as ex:
-            futs = {n: ex.submit(_compile, n, s) for n, s in todo.items()}
+            futs = {n: ex.submit(_compile, n, src, extra) for n, (src, extra) in todo.items()}
             for n, f in futs.items():
                 _, log = f.result()
                 if verbose:

@@ -310,15 +310,58 @@ struct OrderWalk {
 
 __device__ int g_status;  // sticky: 0 = fine, else the site of the first wait that ran out
 
+#ifdef ATTN_TRACE
+// Timeline build (-DATTN_TRACE, off by default): lane 0 of each role records
+// (%globaltimer, event, argument) at the points below, in a fixed device array
+// that attn_fwd_trace_read copies out.  Event codes and roles are listed in
+// attn_fwd_trace.h.  Without the switch every trace point compiles to nothing.
+constexpr int kTraceRoles = 5;      // producer, issuer, softmax tile 0, softmax tile 1, store warp
+constexpr int kTraceEvents = 2048;  // per role and CTA; later events are counted but not kept
+constexpr int kTraceCtas = 160;     // CTAs numbered past this are not recorded
+struct TraceRec {
+  unsigned long long t;
+  unsigned int code;
+  unsigned int arg;
+};
+__device__ TraceRec g_trace[kTraceCtas * kTraceRoles * kTraceEvents];
+__device__ unsigned int g_trace_n[kTraceCtas * kTraceRoles];
+struct Tracer {
+  int role;
+  bool on;  // the recording lane
+  unsigned int n;
+  __device__ __forceinline__ void rec(unsigned int code, unsigned int arg) {
+    if (!on) return;
+    if (blockIdx.x < kTraceCtas && n < kTraceEvents)
+      g_trace[(blockIdx.x * kTraceRoles + role) * kTraceEvents + n] = TraceRec{global_timer_ns(), code, arg};
+    ++n;
+  }
+  __device__ __forceinline__ void done() {
+    if (on && blockIdx.x < kTraceCtas) g_trace_n[blockIdx.x * kTraceRoles + role] = n;
+  }
+};
+#define ATTN_TR_DECL(role, on) Tracer tr_{(role), (on), 0u}
+#define ATTN_TR(code, arg) tr_.rec((code), static_cast<unsigned int>(arg))
+#define ATTN_TR_DONE() tr_.done()
+#else
+#define ATTN_TR_DECL(role, on) ((void)0)
+#define ATTN_TR(code, arg) ((void)0)
+#define ATTN_TR_DONE() ((void)0)
+#endif
+
 // Dynamic schedule.  CTA c starts on item c; later items are claimed in list
 // order (heaviest first) from a counter, so a CTA that finishes early takes the
 // next item and the CTAs end within about one (small) item of each other.  Each
-// launch uses one of kSchedSlots counters, chosen by the host in turn.  Every CTA
+// launch uses one of kSchedSlots counters, chosen by the host: launches made
+// directly take the first kEagerSlots in turn, launches recorded into a CUDA graph
+// (stream capture) the remaining ones in turn, so a graph's launches, which keep
+// the counter they were recorded with, never share one with a direct launch.  Every CTA
 // claims until a claim comes back past the last item, so a launch makes exactly
 // n_items claims (a CTA that unwinds early makes the rest of its claims before it
 // exits); the claim numbered n_items - 1 is the launch's last, and its taker
 // returns the counter to zero, with no end-of-kernel synchronisation.
-constexpr int kSchedSlots = 64;
+constexpr int kEagerSlots = 64;
+constexpr int kCaptureSlots = 4096;
+constexpr int kSchedSlots = kEagerSlots + kCaptureSlots;
 __device__ int g_sched_next[kSchedSlots];
 constexpr int kSeqSlots = 4;  // depth of the shared-memory ring through which the producer publishes items
 constexpr int kSeqConsumers = 10;  // warps reading the ring: eight softmax warps, the issuer, the store warp
@@ -425,6 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1)
    regs_decrease<kRegsOther>();
    if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
+    ATTN_TR_DECL(0, lane == 0);
+    ATTN_TR(0, 0);  // CTA start
     if (lane == 0) {
       tma_prefetch_map(&tq);
       tma_prefetch_map(&tk);
@@ -453,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&seq_full[k % kSeqSlots]);
       }
       __syncwarp();
+      ATTN_TR(1, more ? x : -1);  // item published
       if (!more) break;
       const Item it = item_at<SPLIT, SPARSE>(p, x);
       const int n_tiles = LISTED ? n_marked : it.n_tiles;
@@ -518,6 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cb = 0; cb < D / 64; ++cb)
           tma_load_3d_elect(kv_s + slot * C::kTileBytes + cb * C::kColBlockBytes, map, &kv_full[slot], cb * 64,
                             kb * BN, it.kv_z);
+        ATTN_TR((i & 1) ? 3 : 2, kb);  // V or K load issued
         ++kv_it;
       }
       if (ok) x = claim();
@@ -538,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t i = (kv_it > S ? kv_it - S : 0); i < kv_it; ++i)
         mbar_wait_bounded(&kv_full[i % S], (i / S) & 1, abort_v, kDrainTimeoutNs);
     }
+    ATTN_TR_DONE();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tcgen05 issuer
     const uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
@@ -574,6 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_v = [&](uint32_t n) {
       return warp_wait(&v_ready[n % S], (n / S) & 1, abort_v, kTimeoutNs);
     };
+    ATTN_TR_DECL(1, lane == 0);
     uint32_t kv_it = 0;   // K/V loads consumed
     uint32_t g = 0;       // key tiles processed over all items (p_full phase)
     uint32_t n_done = 0;  // items with key tiles processed
@@ -590,6 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kslot = kv_it % S;
       ++kv_it;
       tc_fence_after();
+      ATTN_TR(12, x);  // item start: its first S products
       issue_s(0, kslot, smem_u32(&s_full[0]));
       issue_s(1, kslot, smem_u32(&s_full[1]), smem_u32(&kv_empty[kslot]));
       if (n == 1) mma_commit_elect(&q_empty);
@@ -621,6 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // the last P.V of O_0 completes it: its epilogue can start
         issue_pv(0, vslot, !first, last ? smem_u32(&o_final[0]) : kNoBar);
+        ATTN_TR(11, 0);
         if constexpr (!last) issue_s(0, ks, smem_u32(&s_full[0]));
         if constexpr (first) {
           if (n_done > 0) good = warp_wait(&o_empty[1], (n_done - 1) & 1, abort_v, kTimeoutNs);
@@ -629,6 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!good) return false;
         tc_fence_after();
         issue_pv(1, vslot, !first, last ? smem_u32(&o_final[1]) : kNoBar, smem_u32(&kv_empty[vslot]));
+        ATTN_TR(11, 1);
         if constexpr (!last) {
           issue_s(1, ks, smem_u32(&s_full[1]), smem_u32(&kv_empty[ks]));
           if constexpr (qlast) mma_commit_elect(&q_empty);  // that was the item's last S
@@ -658,6 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           // the last P.V of O_0 completes it: its epilogue can start
           issue_pv(0, vslot, j > 0, j + 1 == n ? smem_u32(&o_final[0]) : kNoBar);
+          ATTN_TR(11, 0);  // P.V of Q tile 0 issued
           const bool more = j + 1 < n;
           if (more) {
             kslot = kv_it % S;
@@ -672,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           issue_pv(1, vslot, j > 0, j + 1 == n ? smem_u32(&o_final[1]) : kNoBar, smem_u32(&kv_empty[vslot]));
+          ATTN_TR(11, 1);  // P.V of Q tile 1 issued
           if (more) {
             issue_s(1, kslot, smem_u32(&s_full[1]), smem_u32(&kv_empty[kslot]));
             if (j + 2 == n) mma_commit_elect(&q_empty);  // that was the item's last S
@@ -686,12 +740,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every MMA issued above has completed before TMEM can be freed
     mma_commit_elect(&mma_drain);
     warp_wait(&mma_drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
+    ATTN_TR(13, 0);  // every MMA of the CTA has completed
+    ATTN_TR_DONE();
    } else if (warp == kStoreWarp) {
     // ------------------------------------------------------------ O stores
     // Once a Q tile's epilogue has staged O (stage_full), one TMA store per 64
     // columns writes it out; the staging buffer is handed back (stage_rel) when the
     // stores have read it.  The softmax warps never wait for a store.
     uint32_t e_seen[QTILES] = {0, 0};
+    ATTN_TR_DECL(4, lane == 0);
     bool ok = true;
     for (int k = 0; ok; ++k) {
       int x, n_marked = 0;
@@ -709,6 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cb = 0; cb < D / 64; ++cb)
             tma_store_3d_elect(&to, stage + cb * (BM * 128), cb * 64, it.q0 + t * BM, it.bh);
           bulk_commit_group_elect();
+          ATTN_TR(30, t);  // O stores of Q tile t issued
           bulk_wait_group_read0();  // the staging tile has been read: hand it on
           __syncwarp();
           if (lane == 0) mbar_arrive(&stage_rel[t]);
@@ -717,12 +775,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) record_abort(abort_v, kSiteEpilogue);
     bulk_wait_group0();  // every store has landed before the CTA exits
+    ATTN_TR(31, 0);
+    ATTN_TR_DONE();
    }
   } else {
     // ------------------------------------------------------------ softmax (+ rescale, epilogue)
     regs_increase<kRegsSoftmax>();
     const int t = warp / 4;
     const int quarter = warp % 4;
+    ATTN_TR_DECL(2 + t, quarter == 0 && lane == 0);
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + t * BN;
     const uint32_t o_tmem = tmem + lane_off + 2 * BN + t * 128;
@@ -833,9 +894,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();  // this thread's writes are visible to the tensor cores' reads
           __syncwarp();
           if (lane == 0) mbar_arrive(&v_ready[vn % S]);
+          ATTN_TR(22, j);  // this thread's share of V_j converted
         }
         ok = warp_wait(&s_full[t], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
+        ATTN_TR(20, j);  // S_t(j) ready
         tc_fence_after();
         if constexpr (SPARSE) {
           // block-sparse mode: a tile no row of this warp sees (one only the other Q tile's
@@ -850,6 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&p_full[t]);
+            ATTN_TR(21, j);
             continue;
           }
         }
@@ -1017,6 +1081,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
+        ATTN_TR(21, j);  // P_t(j) handed to the MMA
         if constexpr (!C::kTensorRowSum) {  // the sum of the fp16-rounded P, after the hand-off
           float q0 = 0.0f, q1 = 0.0f, q2 = 0.0f, q3 = 0.0f;
 #pragma unroll
@@ -1060,6 +1125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&o_empty[t]);  // O_t may now be overwritten by the next item's first P.V
+      ATTN_TR(23, x);  // O_t read out of TMEM
       const bool any_key = l > 0.0f;
       const float inv_l = any_key ? 1.0f / l : 0.0f;
       if (SPLIT) {  // fp32 partial O (normalised by this range's l) and partial LSE, for the merge
@@ -1113,8 +1179,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();  // this thread's staged row is visible to the TMA store
       mbar_arrive(&stage_full[t]);  // the store warp writes the tile out
+      ATTN_TR(24, x);  // O_t staged
       if (live) *lrow = any_key ? (m + lg2_approx(l_exact)) * 0.69314718055994531f : -INFINITY;
     }
+    ATTN_TR_DONE();
   }
 
   tc_fence_before();
@@ -1136,7 +1204,8 @@ int cuda_fail(cudaError_t e) {
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<unsigned int> g_launch_seq{0};  // picks each launch's schedule counter
+std::atomic<unsigned int> g_launch_seq{0};   // picks each direct launch's schedule counter
+std::atomic<unsigned int> g_capture_seq{0};  // picks each captured launch's schedule counter
 std::mutex g_dev_mutex;
 int g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 unsupported
 int g_dev_sms[kMaxDevices];    // streaming multiprocessors per device
@@ -1245,7 +1314,7 @@ struct Launch {
 };
 
 int prepare_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
-                   int Sk, int D, int causal, float scale, int n_splits, Launch* L) {
+                   int Sk, int D, int causal, float scale, int n_splits, cudaStream_t stream, Launch* L) {
   // ---- argument checks (host only, before any CUDA call)
   if (B < 0 || Sq < 0 || Sk < 0 || Hq < 1 || Hkv < 1) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_INVALID_ARG;
@@ -1309,7 +1378,15 @@ int prepare_launch(const void* q, const void* k, const void* v, void* o, float* 
   prm.n_splits = n_splits;
   prm.o_part = nullptr;
   prm.lse_part = nullptr;
-  prm.sched_slot = static_cast<int>(g_launch_seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+  {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return cuda_fail(e);
+    prm.sched_slot = (cs == cudaStreamCaptureStatusActive)
+                         ? kEagerSlots + static_cast<int>(g_capture_seq.fetch_add(1, std::memory_order_relaxed) %
+                                                          kCaptureSlots)
+                         : static_cast<int>(g_launch_seq.fetch_add(1, std::memory_order_relaxed) % kEagerSlots);
+  }
   prm.mask = nullptr;
   prm.order = nullptr;
   prm.order_heads = 1;
@@ -1356,24 +1433,56 @@ int run_splitkv(const Launch& L0, void* ws, int64_t rows, int D, cudaStream_t st
 // Fixed scratch for attn_fwd_splitkv_noalloc: the split-key partials of callers
 // that cannot allocate device memory.  Every device that loads this library
 // holds these 32 MiB until the process exits.  Host code only uses the name to
-// look up the device address (cudaGetSymbolAddress), once per device.
+// look up the device address (cudaGetSymbolAddress), once per CUDA context.
 constexpr size_t kNoAllocScratchBytes = size_t{32} << 20;
 static __device__ __align__(256) unsigned char g_splitkv_scratch[kNoAllocScratchBytes];
 
 namespace {
 
 std::mutex g_scratch_mutex;
-void* g_scratch_addr[kMaxDevices];  // device address of g_splitkv_scratch, per device
+void* g_scratch_addr[kMaxDevices];                // device address of g_splitkv_scratch, per device
+unsigned long long g_scratch_ctx[kMaxDevices];    // ... and the id of the context it was looked up in
 
-// Device address of the fixed scratch on `dev` (the current device); looked up on first use.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (ids are never reused within
+// a process, so a context created after a cudaDeviceReset gets a new one); false
+// when the driver does not provide it.
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the fixed scratch on `dev` (the current device), looked up on
+// the first call in each context: an address from an earlier context (before a
+// cudaDeviceReset, say) is never reused.
 int noalloc_scratch(int dev, void** out) {
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  unsigned long long ctx = 0;
+  const bool have_ctx = current_context_id(&ctx);
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (g_scratch_addr[dev] == nullptr || !have_ctx || g_scratch_ctx[dev] != ctx) {
     void* ptr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&ptr, g_splitkv_scratch);
     if (e != cudaSuccess) return cuda_fail(e);
     g_scratch_addr[dev] = ptr;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_addr[dev];
   return ATTN_OK;
@@ -1386,7 +1495,7 @@ extern "C" {
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
              int Sk, int D, int causal, float scale, cudaStream_t stream) {
   Launch L;
-  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, 1, &L);
+  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, 1, stream, &L);
   if (st != ATTN_OK || L.empty) return st;
   return D == 128 ? launch<128, false>(L, stream) : launch<64, false>(L, stream);
 }
@@ -1414,7 +1523,7 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
                      int Sq, int Sk, int D, int causal, float scale, int n_splits, void* workspace,
                      size_t workspace_bytes, cudaStream_t stream) {
   Launch L;
-  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, n_splits, &L);
+  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, n_splits, stream, &L);
   if (st != ATTN_OK || L.empty) return st;
   const int64_t rows = static_cast<int64_t>(B) * Hq * Sq;
   if (!workspace) return ATTN_ERR_NULL_PTR;
@@ -1452,7 +1561,7 @@ int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, f
     }
   }
   Launch L;
-  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, 1, &L);
+  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, 1, stream, &L);
   if (st != ATTN_OK || L.empty) return st;
   L.prm.mask = block_mask;
   L.prm.mask_heads = mask_heads;
@@ -1483,7 +1592,7 @@ int attn_fwd_ordered(const void* q, const void* k, const void* v, void* o, float
     }
   }
   Launch L;
-  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, 1, &L);
+  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, 1, stream, &L);
   if (st != ATTN_OK || L.empty) return st;
   L.prm.order = tile_order;
   L.prm.order_heads = order_heads;
@@ -1495,7 +1604,7 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
                              int Hkv, int Sq, int Sk, int D, int causal, float scale, int n_splits,
                              cudaStream_t stream) {
   Launch L;
-  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, n_splits, &L);
+  const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, n_splits, stream, &L);
   if (st != ATTN_OK || L.empty) return st;
   const int64_t rows = static_cast<int64_t>(B) * Hq * Sq;
   if (splitkv_bytes(rows, D, n_splits, nullptr) > kNoAllocScratchBytes) return ATTN_ERR_INVALID_ARG;
@@ -1506,6 +1615,24 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
   // so what an earlier call left in the scratch is never read: nothing to clear.
   return run_splitkv(L, scratch, rows, D, stream);
 }
+
+#ifdef ATTN_TRACE
+int attn_fwd_trace_read(void* dst, size_t dst_bytes, int* ctas, int* roles, int* events) {
+  if (ctas) *ctas = kTraceCtas;
+  if (roles) *roles = kTraceRoles;
+  if (events) *events = kTraceEvents;
+  const size_t n_bytes = sizeof(unsigned int) * kTraceCtas * kTraceRoles;
+  const size_t r_bytes = sizeof(TraceRec) * static_cast<size_t>(kTraceCtas) * kTraceRoles * kTraceEvents;
+  if (!dst) return ATTN_ERR_NULL_PTR;
+  if (dst_bytes < n_bytes + r_bytes) return ATTN_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(dst, g_trace_n, n_bytes);
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(static_cast<uint8_t*>(dst) + n_bytes, g_trace, r_bytes);
+  static const unsigned int zeros[kTraceCtas * kTraceRoles] = {};  // the next launch starts from empty counts
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_trace_n, zeros, n_bytes);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+#endif
 
 const char* attn_fwd_strerror(int status) {
   switch (status) {

@@ -4,7 +4,10 @@
 //   * S = Q K^T with both operands K-major in shared memory (SS form), the
 //     accumulator read back from tensor memory with tcgen05.ld;
 //   * O = P V with P written into tensor memory by tcgen05.st (TS form) and V
-//     MN-major in shared memory.
+//     MN-major in shared memory;
+// and two rate probes: the dense bf16 tcgen05 MMA rate per SM and the ex2.approx
+// rate per SM, behind the peak and the softmax bound the benchmark and the
+// kernel's design use.
 // Each runs as a single CTA of 128 threads on one 128-row tile; the tests
 // compare the results with CPU matmuls.  Test infrastructure for the library
 // (declared in include/attn_fwd_probe.h), not part of the attention path.
@@ -201,6 +204,84 @@ __global__ void __launch_bounds__(64, 1) probe_wait_timeout_kernel(uint64_t time
   __syncthreads();
 }
 
+// Dense bf16 MMA rate: one thread issues n back-to-back tcgen05 MMAs of 128 x N x 16
+// (A 128 rows and B N rows, K-major, 128-byte swizzled, zero-filled shared memory),
+// accumulating into one TMEM tile, then waits for them; the CTA's clock64 and
+// %globaltimer spans give the rate per SM and the clock.  The dynamic shared
+// memory keeps one CTA per SM.
+__global__ void __launch_bounds__(128, 1) probe_mma_rate_kernel(int n, int N, unsigned long long* cycles,
+                                                                unsigned long long* nanos, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  uint8_t* a_s = smem;              // 128 rows x 128 B
+  uint8_t* b_s = smem + 128 * 128;  // N rows x 128 B
+  __shared__ uint64_t bar_mma;
+  __shared__ uint32_t tmem_base;
+  __shared__ uint32_t abort_flag;
+  const int warp = threadIdx.x / 32;
+  for (int i = threadIdx.x; i < (128 + N) * 128 / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_mma, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+  if (threadIdx.x == 0) {
+    const uint32_t idesc = idesc_bf16_f32(128, N, false);
+    const uint64_t t0 = global_timer_ns();
+    const long long c0 = clock64();
+    for (int i = 0; i < n; ++i) {
+      const uint32_t off = (i % 4) * 32;  // the four K steps of one 128-byte swizzle span
+      mma_bf16_ss(tbase, sdesc_sw128(smem_u32(a_s) + off, 16, 1024), sdesc_sw128(smem_u32(b_s) + off, 16, 1024),
+                  idesc, i > 0 ? 1u : 0u);
+    }
+    mma_commit(&bar_mma);
+    const bool ok = mbar_wait_bounded(&bar_mma, 0, &abort_flag, kProbeTimeoutNs);
+    const long long c1 = clock64();
+    const uint64_t t1 = global_timer_ns();
+    cycles[blockIdx.x] = static_cast<unsigned long long>(c1 - c0);
+    nanos[blockIdx.x] = t1 - t0;
+    if (!ok) atomicExch(status, 2);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 256);
+  }
+}
+
+// ex2.approx rate: every thread runs 8 independent chains x <- 2^x - 1.5 (the
+// subtraction, on the FMA pipe, keeps x bounded), `iters` steps each.
+__global__ void __launch_bounds__(512, 1) probe_ex2_rate_kernel(int iters, unsigned long long* cycles,
+                                                                float* sink) {
+  float x[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) x[c] = 0.01f * (threadIdx.x % 7) + 0.1f * c;
+  __syncthreads();
+  const long long c0 = clock64();
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) x[c] = ex2_approx(x[c]) - 1.5f;
+  }
+  __syncthreads();
+  const long long c1 = clock64();
+  float acc = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) acc += x[c];
+  sink[blockIdx.x * blockDim.x + threadIdx.x] = acc;
+  if (threadIdx.x == 0) cycles[blockIdx.x] = static_cast<unsigned long long>(c1 - c0);
+}
+
 int launch_status(cudaError_t e) { return e == cudaSuccess ? 0 : 100 + static_cast<int>(e); }
 
 }  // namespace
@@ -241,6 +322,24 @@ int attn_probe_wait_timeout(unsigned long long timeout_ns, unsigned long long ab
   if (!status || !waited_ns) return 2;
   if (timeout_ns == 0 || timeout_ns > 2000000000ull || abort_after_ns > 2000000000ull) return 1;
   probe_wait_timeout_kernel<<<1, 64, 0, stream>>>(timeout_ns, abort_after_ns, status, waited_ns);
+  return launch_status(cudaGetLastError());
+}
+
+int attn_probe_mma_rate(int n_mma, int N, int grid, unsigned long long* cycles, unsigned long long* nanos,
+                        int* status, cudaStream_t stream) {
+  if (!cycles || !nanos || !status) return 2;
+  if (n_mma < 1 || n_mma > (1 << 20) || (N != 64 && N != 128 && N != 256) || grid < 1 || grid > 1024) return 1;
+  const int smem = 200 * 1024;  // one CTA per SM (the operands need 48 KB at most)
+  cudaError_t e = cudaFuncSetAttribute(probe_mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return launch_status(e);
+  probe_mma_rate_kernel<<<grid, 128, smem, stream>>>(n_mma, N, cycles, nanos, status);
+  return launch_status(cudaGetLastError());
+}
+
+int attn_probe_ex2_rate(int iters, int grid, unsigned long long* cycles, float* sink, cudaStream_t stream) {
+  if (!cycles || !sink) return 2;
+  if (iters < 1 || iters > (1 << 20) || grid < 1 || grid > 1024) return 1;
+  probe_ex2_rate_kernel<<<grid, 512, 0, stream>>>(iters, cycles, sink);
   return launch_status(cudaGetLastError());
 }
 

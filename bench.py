@@ -42,6 +42,9 @@ from attention_forward_06_gb300.inputs import (WORKLOADS, Workload, bf16_bits, b
 METRIC = "attn fwd TFLOPS (bf16, 1×GB300) and % of dense-BF16 tensor peak; geomean"
 PERF_WORKLOADS = ["train", "gqa", "chunked128", "chunked64", "long"]
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+# Dense bf16 tensor-core work one SM completes per clock: one 128 x 256 x 16 tcgen05 MMA (1 048 576 FLOP) per 128
+# cycles, as the MMA-rate probe (attn_probe_mma_rate, tests/test_probe.py) measures on GB300.
+BF16_FLOP_PER_CLK_PER_SM = 8192
 KERNEL_SOURCES = ["attention_forward_06_gb300/csrc/attn_fwd.cu", "attention_forward_06_gb300/csrc/ptx.cuh"]
 
 
@@ -214,28 +217,100 @@ def traffic_for(workload: str):
     return entry.get("dram_bytes_per_launch")
 
 
-def cpu_baseline(w: Workload, budget_s: float = 12.0) -> dict:
-    """The oracle, as it stands, on sampled rows of the workload, for about budget_s seconds."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or 'unknown'."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def oracle_rows(w: Workload, budget_s: float, seed: int):
+    """The oracle, as it stands, on rows drawn uniformly per (batch, head) in rounds of doubling size for about
+    budget_s seconds: (rows, o [n, D], lse [n], FLOP, seconds)."""
     import oracle  # test infrastructure: timed here as the CPU baseline only
 
     q, k, v = draw_workload(w)
     qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
-    flops, elapsed, nrows, chunk = 0.0, 0.0, 0, 1
-    seed = w.seed + 2000
+    flops, elapsed, chunk = 0.0, 0.0, 1
+    rows_all, o_all, l_all = [], [], []
     while elapsed < budget_s:
         rows = sample_rows(w.B, w.Hq, w.Sq, chunk, seed=seed)
         seed += 1
         t0 = time.perf_counter()
-        oracle.attention(qb, kb, vb, w.causal, w.scale, rows=rows)
+        o, lse = oracle.attention(qb, kb, vb, w.causal, w.scale, rows=rows)
         dt = time.perf_counter() - t0
         elapsed += dt
         flops += row_flops(w, rows)
-        nrows += len(rows)
+        rows_all.append(rows)
+        o_all.append(o)
+        l_all.append(lse)
         if dt < budget_s / 8:
             chunk = min(chunk * 2, w.Sq)
-    return {"value": flops / elapsed / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{nrows} query rows in total, drawn uniformly per (batch, head) in rounds, of the {w.name} "
-                      f"workload ({flops:.3g} FLOP, {elapsed:.1f} s, fp64)"}
+    return np.concatenate(rows_all), np.concatenate(o_all), np.concatenate(l_all), flops, elapsed
+
+
+def sampled_parity(o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray) -> dict:
+    """The parity rule of the tests on sampled rows: |dO| <= 1e-2 where |O_ref| < 4 (some bf16 value lies within
+    2^-7 there), the excess over the bf16 rounding floor <= 1e-2 from 4 upwards, |dLSE| <= 1e-3."""
+    d = np.abs(o_gpu - o_ref)
+    small = np.abs(o_ref) < 4.0
+    _, ex = np.frexp(np.abs(o_ref[~small]))  # the exact result rounded to bf16 (8 significant bits)
+    spacing = np.ldexp(1.0, ex - 8)
+    floor = np.abs(np.round(np.abs(o_ref[~small]) / spacing) * spacing - np.abs(o_ref[~small]))
+    excess = d[~small] - floor
+    live = np.isfinite(lse_ref)
+    dl = np.abs(lse_gpu[live] - lse_ref[live])
+    out = {"rows": int(o_ref.shape[0]), "max_abs_dO": float(d.max()) if d.size else 0.0,
+           "max_abs_dO_below_4": float(d[small].max()) if small.any() else 0.0,
+           "max_excess_dO_from_4": float(excess.max()) if excess.size else 0.0,
+           "max_abs_dLSE": float(dl.max()) if dl.size else 0.0}
+    out["plain_dO_within_1e-2"] = out["max_abs_dO_below_4"] <= 1e-2
+    out["within_tolerance"] = (out["plain_dO_within_1e-2"] and out["max_excess_dO_from_4"] <= 1e-2
+                               and out["max_abs_dLSE"] <= 1e-3)
+    return out
+
+
+def cpu_baseline(w: Workload, outputs: dict, budget_s: float = 8.0, other_budget_s: float = 3.0) -> dict:
+    """The oracle, as it stands, on the machine's host cores: the headline workload for about budget_s seconds and
+    every other workload whose GPU output is in `outputs` for about other_budget_s seconds.  Each gives the
+    oracle's rate, the seconds the whole workload would take at that rate (extrapolated) and, where the GPU's
+    output rows are at hand, the parity of those rows under the tests' rule."""
+    import oracle
+
+    per = {}
+    names = [w.name] + [n for n in outputs if n != w.name]
+    for name in names:
+        wx = WORKLOADS[name]
+        rows, o_ref, l_ref, flops, secs = oracle_rows(wx, budget_s if name == w.name else other_budget_s,
+                                                      wx.seed + 2000)
+        entry = {"tflops": flops / secs / 1e12, "rows": int(rows.size), "seconds": secs,
+                 "full_config_s_extrapolated": alg_flops(wx) / (flops / secs)}
+        if name in outputs:
+            o_gpu, l_gpu = outputs[name]  # host copies of the GPU's outputs, [B, Hq, Sq, D] bf16 and [B, Hq, Sq]
+            idx = torch.from_numpy(rows)
+            entry["parity"] = sampled_parity(o_gpu.reshape(-1, wx.D)[idx].double().numpy(),
+                                             l_gpu.reshape(-1)[idx].double().numpy(), o_ref, l_ref)
+        per[name] = entry
+    head = per[w.name]
+    return {"value": head["tflops"], "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "sample": f"{head['rows']} query rows in total, drawn uniformly per (batch, head) in rounds, of the "
+                      f"{w.name} workload ({head['seconds']:.1f} s, fp64); the other workloads for about "
+                      f"{other_budget_s:g} s each; full_config_s_extrapolated = the workload's algorithmic FLOP at "
+                      f"the measured rate",
+            "per_workload": per}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -362,6 +437,14 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (statistics.mean(times) * 1e-3) / 1e12
+    # the tensor cores' own rate: SMs x dense bf16 FLOP per clock per SM x clock, at the maximum SM clock and at
+    # the median SM clock sampled during the timed region
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    hw = {}
+    for key, mhz in (("at_max_clock", (clocks or {}).get("sm_max_mhz")), ("at_median_clock", (clocks or {}).get("sm_mhz"))):
+        if mhz:
+            hw[key] = {"sm_mhz": mhz, "peak_tflops": sms * BF16_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12}
+            hw[key]["frac"] = achieved / hw[key]["peak_tflops"]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -371,14 +454,20 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
                    "alg_flop_per_step": flops, "conv_flop_per_step": conv_flops(w),
                    "tflops_conv": job_tflops(conv_flops(w), world, args.steps, total_ms),
                    "pct_of_peak": 100.0 * achieved / peak,
+                   "headline": "the line's value is this training-prefill workload; geomean_tflops is the geomean "
+                               "of the five performance workloads (train, gqa, chunked128, chunked64, long)",
                    "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_source": f"{peak_kind} bf16_tflops (burst: kernel timed alone)",
+                     "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} bf16_tflops: cuBLAS-achieved bf16 matmul (burst; the kernel is "
+                                    f"timed alone), of measured",
+                     "peak_hw": {"sms": sms, "bf16_flop_per_clk_per_sm": BF16_FLOP_PER_CLK_PER_SM, **hw},
                      "traffic": traffic_for(w.name), "alg_hbm_bytes": min_hbm_bytes(w)},
         "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
+    outputs = {w.name: (od.cpu(), lsed.cpu())}  # host copies of the GPU's outputs, for the sampled parity check
     if not args.skip_workloads:
         per, detail = {}, {}
         for name in ["tiny"] + PERF_WORKLOADS:
@@ -393,7 +482,9 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
                 def fx():
                     ops.attn_fwd(qx, kx, vx, causal=wx.causal, scale=wx.scale, o=ox, lse=lx, stream=stream)
 
-                ms = statistics.mean(time_kernel(fx, min(args.steps, 10), 2, flush, stream))
+                ms = statistics.mean(time_kernel(fx, min(args.steps, 10), 3, flush, stream))
+                if name in PERF_WORKLOADS:
+                    outputs[name] = (ox.cpu(), lx.cpu())
                 del qx, kx, vx, ox, lx
             alg = alg_flops(wx) / (ms * 1e-3) / 1e12
             if name in PERF_WORKLOADS:
@@ -403,6 +494,11 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
             detail[name] = {"ms": ms, "tflops_alg": alg, "tflops_conv": conv_flops(wx) / (ms * 1e-3) / 1e12,
                             "pct_of_peak_alg": 100.0 * alg / peak,
                             "alg_hbm_gbs": min_hbm_bytes(wx) / (ms * 1e-3) / 1e9}
+            # DRAM bytes of one launch from the committed ncu capture (null once the kernel has changed since), and
+            # the HBM throughput they make at this launch time
+            traffic = traffic_for(name)
+            detail[name]["traffic"] = traffic
+            detail[name]["dram_gbs"] = traffic / (ms * 1e-3) / 1e9 if traffic else None
         line["per_workload_tflops"] = per
         line["per_workload"] = detail
         line["tiny_latency_us"] = 1e3 * detail["tiny"]["ms"]
@@ -415,7 +511,7 @@ def run_ours(args, w: Workload, rank: int, world: int, dist):
         line["splitkv"] = bench_splitkv(stream, flush, dev, min(args.steps, 10))
         line["ordered"] = bench_ordered(stream, flush, dev, min(args.steps, 10))
     if world == 1 and not args.skip_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, outputs)
     return line
 
 

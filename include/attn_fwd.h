@@ -37,6 +37,17 @@
  * not modified.  Calls are re-entrant; the one-time initialisation (driver
  * entry point, per-device capability check and kernel attributes) is guarded.
  *
+ * Concurrency.  Each forward launch (attn_fwd and every variant below) claims
+ * its work items from one of a set of device counters and returns that counter
+ * to zero as it finishes.  Launches made directly take 64 counters in turn;
+ * launches recorded into a CUDA graph (stream capture) take another 4096 in turn
+ * and keep theirs for every replay.  So: at most 64 direct launches may be in
+ * flight on one device at once (on different streams); a direct launch never
+ * shares a counter with a recorded one; and launches recorded 4096 or more
+ * captures apart may share one, so graphs holding them must not run at the same
+ * time.  Two launches that did share a counter while running would silently
+ * skip or repeat work items.
+ *
  * Precision.  bf16 inputs; both products accumulate in fp32 on the tensor
  * cores; softmax in fp32 with exp2.  The P.V product runs in fp16: P is rounded
  * to fp16 (nearest-even) and the normaliser sums those same rounded values, and
@@ -124,9 +135,10 @@ int attn_fwd_splitkv_suggest(int B, int Hq, int Sq, int Sk, int D, int causal);
  * workspace: calls whose n_splits * B*Hq*Sq * (D + 1) * 4 bytes (plus up to 255
  * bytes of alignment) exceed 32 MiB are rejected with ATTN_ERR_INVALID_ARG
  * before any device work.  Nothing is allocated: every GPU that loads the
- * library holds the 32 MiB until the process exits.  The first call on a device
- * looks up the array's device address there (once; a host-side query), so make
- * that first call before any stream capture.  All calls share the one array and
+ * library holds the 32 MiB until the process exits.  The first call in each
+ * CUDA context looks up the array's device address there (a host-side query;
+ * again after a cudaDeviceReset, which ends the context), so make that first
+ * call before any stream capture.  All calls share the one array and
  * each call overwrites what it needs (nothing has to start at zero), so calls
  * that overlap on the GPU -- on different streams, or on the same device from
  * different threads without ordering -- race and must be serialised by the caller.

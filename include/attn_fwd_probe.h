@@ -51,6 +51,25 @@ int attn_probe_mma_ts(const void* p, const void* v, int D, int lbo, int sbo, flo
 int attn_probe_wait_timeout(unsigned long long timeout_ns, unsigned long long abort_after_ns, int* status,
                             unsigned long long* waited_ns, cudaStream_t stream);
 
+/*
+ * Dense bf16 tensor-core rate: `grid` CTAs (one per SM) each issue n_mma
+ * back-to-back tcgen05 MMAs of 128 x N x 16 (N = 64, 128 or 256) from one
+ * thread into one TMEM accumulator and wait for them.  cycles[c] / nanos[c]
+ * (device memory, `grid` entries each) receive CTA c's clock64 and %globaltimer
+ * spans: 2 * 128 * N * 16 * n_mma / cycles is the dense bf16 FLOP per clock of an
+ * SM, cycles / nanos its clock in GHz.  *status = 2 if the wait ran out.
+ */
+int attn_probe_mma_rate(int n_mma, int N, int grid, unsigned long long* cycles, unsigned long long* nanos,
+                        int* status, cudaStream_t stream);
+
+/*
+ * ex2.approx rate: `grid` CTAs of 512 threads, each thread running 8
+ * independent exponential chains for `iters` steps.  cycles[c] receives CTA
+ * c's clock64 span, so 512 * 8 * iters / cycles is the exponentials per clock of
+ * an SM (with one CTA per SM).  sink: grid * 512 floats (keeps the chains).
+ */
+int attn_probe_ex2_rate(int iters, int grid, unsigned long long* cycles, float* sink, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,8 +13,8 @@ from attention_forward_06_gb300 import build as B
 from attention_forward_06_gb300 import _lib, ops
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADERS = {"attn_fwd": "include/attn_fwd.h", "attn_bwd": "include/attn_bwd.h",
-           "attn_probe": "include/attn_fwd_probe.h"}
+HEADERS = {"attn_fwd": "include/attn_fwd.h", "attn_fwd_trace": "include/attn_fwd_trace.h",
+           "attn_bwd": "include/attn_bwd.h", "attn_probe": "include/attn_fwd_probe.h"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,8 +35,19 @@ def test_library_exports_every_declared_symbol(name, built):
     lib = ctypes.CDLL(built[name])
     for f in funcs:
         assert hasattr(lib, f), f"{f} declared in {HEADERS[name]} but not exported"
-    # and the Python binding knows exactly these signatures
-    assert sorted(_lib.SIGNATURES[name]) == funcs
+    # and the Python binding knows exactly these signatures (the traced build exports attn_fwd.h's as well)
+    expected = set(funcs)
+    if name == "attn_fwd_trace":
+        expected |= set(declared_functions(HEADERS["attn_fwd"]))
+        for f in declared_functions(HEADERS["attn_fwd"]):
+            assert hasattr(lib, f), f"{f} missing from the traced build"
+    assert sorted(_lib.SIGNATURES[name]) == sorted(expected)
+
+
+def test_default_build_records_no_timeline(built):
+    lib = ctypes.CDLL(built["attn_fwd"])
+    for f in declared_functions(HEADERS["attn_fwd_trace"]):
+        assert not hasattr(lib, f), f"{f} is exported by the default build"
 
 
 def test_library_is_built_for_sm_103a_only(built):

@@ -55,3 +55,37 @@ def test_forward_splitkv_and_backward_replay_in_a_cuda_graph():
         assert st == ops.ATTN_OK, f"backward wait ran out at site {site}"
         for i, (got, want) in enumerate(zip(out, ref[name])):
             assert torch.equal(got, want), f"output {i} of the replay on input set {name} differs from the eager call"
+
+
+def test_graph_replays_next_to_direct_launches_on_another_stream():
+    """A recorded launch keeps the schedule counter it was given at capture; direct
+    launches draw from a separate set, so a replay running next to many direct
+    launches on another stream (every direct counter taken in turn) shares none."""
+    a = inputs(51)
+    q, k, v = a[:3]
+    o_ref, lse_ref = ops.attn_fwd(q, k, v, causal=CAUSAL, scale=SCALE)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    o_g = torch.full_like(q, float("nan"))
+    lse_g = torch.full(q.shape[:3], float("nan"), device=q.device)
+    with torch.cuda.graph(graph):
+        ops.attn_fwd(q, k, v, causal=CAUSAL, scale=SCALE, o=o_g, lse=lse_g)
+    other = torch.cuda.Stream()
+    direct = []
+    for rep in range(3):
+        o_g.fill_(float("nan"))
+        lse_g.fill_(float("nan"))
+        torch.cuda.synchronize()
+        graph.replay()  # on the current stream
+        with torch.cuda.stream(other):
+            for _ in range(70):  # more than the 64 direct counters
+                o = torch.full_like(q, float("nan"))
+                lse = torch.full(q.shape[:3], float("nan"), device=q.device)
+                ops.attn_fwd(q, k, v, causal=CAUSAL, scale=SCALE, o=o, lse=lse, stream=other)
+                direct.append((o, lse))
+        torch.cuda.synchronize()
+        st, site = ops.debug_status()
+        assert st == ops.ATTN_OK, f"forward wait ran out at site {site}"
+        assert torch.equal(o_g, o_ref) and torch.equal(lse_g, lse_ref), f"replay {rep}"
+    for o, lse in direct:
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)

@@ -85,3 +85,41 @@ def test_ts_mma_p_from_tensor_memory(probe, D):
     if not err < 1e-3:
         alt = (run(1024, 128 * 128) - ref).abs().max().item()
         pytest.fail(f"P.V mismatch: max err {err} (with leading/stride offsets swapped: {alt})")
+
+
+def test_bf16_mma_rate_per_sm(probe):
+    """The dense bf16 tensor-core rate of one SM, measured with back-to-back 128 x N x 16 MMAs on every SM: the
+    per-SM figure behind the benchmark's hardware-derived peak (8192 FLOP per clock)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rates = {}
+    for N in (128, 256):
+        cycles = torch.zeros(sms, dtype=torch.int64, device="cuda")
+        nanos = torch.zeros(sms, dtype=torch.int64, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        n_mma = 4096
+        assert probe.attn_probe_mma_rate(n_mma, N, sms, cycles.data_ptr(), nanos.data_ptr(), status.data_ptr(),
+                                         torch.cuda.current_stream().cuda_stream) == 0
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        c = cycles.cpu().double().numpy()
+        rates[N] = float(np.median(2 * 128 * N * 16 * n_mma / c))
+        ghz = float(np.median(c / nanos.cpu().double().numpy()))
+        print(f"N={N}: {rates[N]:.0f} bf16 FLOP per clock per SM at {ghz:.2f} GHz "
+              f"({rates[N] * sms * ghz * 1e9 / 1e12:.0f} TFLOP/s over {sms} SMs)")
+    assert 0.9 * 8192 <= rates[256] <= 1.05 * 8192
+    assert rates[128] <= 1.05 * 8192
+
+
+def test_ex2_rate_per_sm(probe):
+    """ex2.approx results per clock of one SM (the softmax's exponent unit), every SM busy."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cycles = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    sink = torch.zeros(sms * 512, dtype=torch.float32, device="cuda")
+    iters = 4096
+    assert probe.attn_probe_ex2_rate(iters, sms, cycles.data_ptr(), sink.data_ptr(),
+                                     torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    rate = float(np.median(512 * 8 * iters / cycles.cpu().double().numpy()))
+    print(f"{rate:.1f} ex2.approx per clock per SM")
+    assert torch.isfinite(sink).all()
+    assert 8 <= rate <= 128

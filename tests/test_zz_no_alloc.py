@@ -1,8 +1,9 @@
 """attn_fwd_splitkv_noalloc: the split-key forward for callers that are handed
 only their input and output buffers and may not call cudaMalloc (its partials
 live in a fixed array inside the library).  Called through the C ABI and checked
-against attn_fwd_splitkv, which takes a caller workspace, on two calls in a row;
-the second call uses different inputs so stale scratch contents would show.
+against attn_fwd_splitkv, which takes a caller workspace, on two calls in a row
+(bit for bit: the same kernels run on the same key ranges); the second call uses
+different inputs so stale scratch contents would show.
 """
 import ctypes
 
@@ -13,9 +14,6 @@ from attention_forward_06_gb300 import _lib, ops
 from attention_forward_06_gb300.inputs import draw
 
 pytestmark = pytest.mark.gpu
-
-TOL_O, TOL_LSE = 1e-2, 1e-3
-
 
 @pytest.fixture(scope="module")
 def lib():
@@ -47,8 +45,8 @@ def test_noalloc_matches_workspace_entry_point_twice(lib, shape, causal, n_split
         o_ref, lse_ref = ops.attn_fwd_splitkv(q, k, v, causal=causal, scale=scale, n_splits=n_splits)
         torch.cuda.synchronize()
         assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
-        assert (o.float() - o_ref.float()).abs().max().item() <= TOL_O, f"call {call}"
-        assert (lse - lse_ref).abs().max().item() <= TOL_LSE, f"call {call}"
+        # the same two kernels run on the same key ranges; only where the partials live differs
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref), f"call {call}"
 
 
 def test_noalloc_rejects_work_beyond_its_fixed_scratch(lib):
