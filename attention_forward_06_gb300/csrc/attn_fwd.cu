@@ -35,8 +35,8 @@
 // which keeps the rounding of P four times smaller) and each V tile is converted
 // to fp16 in place in its ring slot before its product, by the softmax warps
 // between one tile's hand-off and the next tile's S (exact for |v| in [2^-14,
-// 65504]; smaller magnitudes round to fp16's subnormal grid, larger ones become
-// infinite).
+// 65504]; smaller magnitudes round to fp16's subnormal grid, larger ones are
+// clamped to +-65504, so masked keys, whose P is 0, never turn a row non-finite).
 //
 // Online softmax per row, in log2 units (c = scale * log2 e), with a lazy
 // reference value m: a tile's exponentials are taken against the current m,

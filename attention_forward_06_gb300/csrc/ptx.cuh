@@ -674,9 +674,14 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 
 // A bf16 pair to the fp16 pair of the same values: exact for magnitudes in
-// [2^-14, 65504], rounded to fp16's subnormal grid below, infinite above.
+// [2^-14, 65504], rounded to fp16's subnormal grid below, clamped to +-65504 above
+// (so a zero weight times an out-of-range value stays zero in a product).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  uint32_t d;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+      : "=r"(d)
+      : "f"(__uint_as_float(w & 0xFFFF0000u)), "f"(__uint_as_float(w << 16)));
+  return d;
 }
 
 // 16-byte shared-memory load and store at a shared-window address.

@@ -54,8 +54,9 @@
  * each V tile is converted to fp16 inside the kernel (exact for magnitudes in
  * [2^-14, 65504]; smaller ones round to fp16's subnormal grid, an absolute
  * error below 2^-25).  V entries beyond 65504 in magnitude are outside the
- * supported range: they become infinite and make the affected O rows
- * non-finite.  O is rounded to bf16 (nearest-even) once, at the end.
+ * supported range: they are clamped to +-65504 in the P.V product, so the rows
+ * that give such a key weight come out wrong (but finite) while every other
+ * row is unaffected.  O is rounded to bf16 (nearest-even) once, at the end.
  */
 #ifndef ATTN_FWD_H
 #define ATTN_FWD_H

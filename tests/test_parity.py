@@ -224,3 +224,36 @@ def test_schedule_counters_across_many_launches():
             assert not torch.isnan(o.float()).any() and not torch.isnan(lse).any(), key
         else:
             assert torch.equal(o, first[key][0]) and torch.equal(lse, first[key][1]), key
+
+
+def test_tiny_v_values_round_to_fp16_subnormals_within_tolerance():
+    # V is converted to fp16 for the P.V product: magnitudes below 2^-14 fall on fp16's subnormal grid
+    # (absolute error below 2^-25), far inside the tolerance; values of every binade down to 2^-30
+    q, k, _ = draw(1, 2, 1, 256, 384, 128, seed=21)
+    g = torch.Generator().manual_seed(22)
+    mag = torch.exp2(-torch.randint(10, 31, (1, 1, 384, 128), generator=g).float())
+    sign = torch.where(torch.rand(1, 1, 384, 128, generator=g) < 0.5, -1.0, 1.0)
+    v = (sign * mag * (1 + torch.rand(1, 1, 384, 128, generator=g))).to(torch.bfloat16)
+    scale = float(np.float32(128 ** -0.5))
+    o, lse = run_gpu(q, k, v, 1, scale)
+    o_ref, lse_ref = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), 1, scale)
+    compare(o, lse, o_ref, lse_ref)
+    assert float(np.abs(o.float().numpy() - o_ref).max()) < 1e-6
+
+
+def test_v_beyond_fp16_range_is_clamped_and_leaves_other_rows_exact():
+    # The documented limit of the fp16 P.V product: a V entry beyond 65504 is clamped to 65504.  The rows
+    # that give its key weight come out wrong but finite; every other row -- including the rows of the same
+    # work items for which the key is masked (their P = 0 multiplies it in the same product) -- is exact.
+    Sq = Sk = 256
+    q, k, v = draw(1, 1, 1, Sq, Sk, 128, seed=23)
+    v = v.clone()
+    v[0, 0, 200, 5] = 1.0e5  # a bf16 value above fp16's largest finite 65504
+    scale = float(np.float32(128 ** -0.5))
+    o, lse = run_gpu(q, k, v, 1, scale)  # causal: rows 0..199 never see key 200
+    o_ref, lse_ref = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), 1, scale)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    compare(o[:, :, :200], lse[:, :, :200], o_ref[:, :, :200], lse_ref[:, :, :200])
+    # the other columns of the rows that see the key are unaffected as well
+    keep = [c for c in range(128) if c != 5]
+    compare(o[:, :, 200:, keep].contiguous(), lse[:, :, 200:], o_ref[:, :, 200:, keep], lse_ref[:, :, 200:])
