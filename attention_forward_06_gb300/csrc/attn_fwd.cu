@@ -61,6 +61,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -1417,7 +1418,10 @@ int launch_merge(const Launch& L, int64_t rows, cudaStream_t stream) {
 }
 
 // Split-key forward with the partials in `ws` (device memory, at least splitkv_bytes).
+// One range is the plain forward: the merge of a single partial multiplies it by
+// exactly 1, so the plain kernel writes the same values without the partials.
 int run_splitkv(const Launch& L0, void* ws, int64_t rows, int D, cudaStream_t stream) {
+  if (L0.prm.n_splits == 1) return D == 128 ? launch<128, false>(L0, stream) : launch<64, false>(L0, stream);
   Launch L = L0;
   size_t lse_off = 0;
   splitkv_bytes(rows, D, L.prm.n_splits, &lse_off);
@@ -1509,14 +1513,42 @@ int attn_fwd_splitkv_suggest(int B, int Hq, int Sq, int Sk, int D, int causal) {
   if (B < 1 || Hq < 1 || Sq < 1 || Sk < 1 || (D != 64 && D != 128) || causal < 0 || causal > 2) return 1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || prepare_device(dev) != ATTN_OK) return 1;
-  const int64_t items = static_cast<int64_t>(B) * Hq * ((Sq + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM);
-  const int64_t sms = g_dev_sms[dev];
-  if (items >= sms) return 1;
-  const int64_t tiles = (Sk + BN - 1) / BN;
-  int64_t splits = (2 * sms + items - 1) / items;     // about two items per SM
-  splits = splits < tiles / 4 ? splits : tiles / 4;   // at least four key tiles per range
-  splits = splits > kMaxSplits ? kMaxSplits : splits;
-  return static_cast<int>(splits < 1 ? 1 : splits);
+  const double sms = g_dev_sms[dev];
+  // Key tiles of every 256-row query block (the work items of one (batch, head)), as the kernel counts them.
+  const int64_t n_qblocks = (Sq + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM;
+  const int64_t diag = causal == 1 ? static_cast<int64_t>(Sk) - Sq : 0;
+  double tiles_sum = 0.0, tiles_max = 0.0;
+  for (int64_t qb = 0; qb < n_qblocks; ++qb) {
+    const int64_t last_row = std::min<int64_t>((qb + 1) * ROWS_PER_ITEM, Sq) - 1;
+    const int64_t kv_end = causal ? std::min<int64_t>(Sk, last_row + diag + 1) : Sk;
+    const double n = kv_end > 0 ? static_cast<double>((kv_end + BN - 1) / BN) : 0.0;
+    tiles_sum += n;
+    tiles_max = std::max(tiles_max, n);
+  }
+  const double items = static_cast<double>(B) * Hq * n_qblocks;
+  if (tiles_max < 8.0) return 1;
+  // Cost model of a launch, calibrated on GB300: a key tile of an item takes t_step, an
+  // item's start and end t_item; the CTAs run the items in waves (ceil(items / SMs) when
+  // the items are about equal, at least the largest one); the partials cost (D + 1)
+  // fp32 per row and range written and read again, plus the output, at an effective
+  // 4 TB/s, and the merge a launch of its own.
+  const double t_step = D == 128 ? 1.55e-6 : 1.2e-6, t_item = 2.5e-6;
+  const double rows = static_cast<double>(B) * Hq * Sq;
+  const double mean_tiles = tiles_sum / n_qblocks;
+  const int s_max = static_cast<int>(std::min<double>(kMaxSplits, tiles_max / 4.0));  // >= 4 key tiles per range
+  int best = 1;
+  double best_cost = 0.0;
+  for (int s = 1; s <= s_max; ++s) {
+    const double waves = std::ceil(items * s / sms);
+    const double makespan = std::max(waves * (mean_tiles / s * t_step + t_item), tiles_max / s * t_step + t_item);
+    const double merge = s > 1 ? 3e-6 + rows * ((D + 1) * 4.0 * s * 2.0 + D * 2.0 + 4.0) / 4e12 : 0.0;
+    const double cost = makespan + merge;
+    if (s == 1 || cost < best_cost * 0.97) {  // a split must gain at least 3 % to be taken
+      best = s;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,

@@ -603,9 +603,28 @@ def bench_splitkv(stream, flush, dev, steps: int) -> dict:
     tp = statistics.mean(time_kernel(fp, steps, 3, flush, stream))
     ts = statistics.mean(time_kernel(fs, steps, 3, flush, stream))
     flops = alg_flops(w)
-    return {"workload": f"{w.label()} (a prefill chunk over a long context)", "n_splits": n_splits,
-            "tflops": flops / (ts * 1e-3) / 1e12, "ms": ts, "plain_ms": tp,
-            "plain_tflops": flops / (tp * 1e-3) / 1e12, "speedup_vs_plain": tp / ts}
+    out = {"workload": f"{w.label()} (a prefill chunk over a long context)", "n_splits": n_splits,
+           "tflops": flops / (ts * 1e-3) / 1e12, "ms": ts, "plain_ms": tp,
+           "plain_tflops": flops / (tp * 1e-3) / 1e12, "speedup_vs_plain": tp / ts}
+    del qx, kx, vx, ox, lx, ws
+    # the chunked workloads through the same entry point with its suggested split count (the last, partly
+    # filled wave of 512 equal items is what a split of the keys evens out)
+    for name in ("chunked128", "chunked64"):
+        wc = WORKLOADS[name]
+        qc, kc, vc = [t.to(dev) for t in draw_workload(wc)]
+        oc = torch.empty_like(qc)
+        lc = torch.empty((wc.B, wc.Hq, wc.Sq), dtype=torch.float32, device=dev)
+        nc = ops.splitkv_suggest(wc.B, wc.Hq, wc.Sq, wc.Sk, wc.D, wc.causal)
+        wsc = torch.empty(ops.splitkv_workspace_size(wc.B, wc.Hq, wc.Sq, wc.D, nc), dtype=torch.uint8, device=dev)
+
+        def fc():
+            ops.attn_fwd_splitkv(qc, kc, vc, causal=wc.causal, scale=wc.scale, n_splits=nc, workspace=wsc, o=oc,
+                                 lse=lc, stream=stream)
+
+        tc = statistics.mean(time_kernel(fc, steps, 3, flush, stream))
+        out[name] = {"n_splits": nc, "ms": tc, "tflops": alg_flops(wc) / (tc * 1e-3) / 1e12}
+        del qc, kc, vc, oc, lc, wsc
+    return out
 
 
 def bench_backward(stream, flush, dev, steps: int, names=("train", "gqa"), warmup: int = 3) -> dict:

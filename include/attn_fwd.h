@@ -106,7 +106,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  * workspace: caller-owned device memory, 16-byte aligned, at least
  * attn_fwd_splitkv_workspace_size(B, Hq, Sq, D, n_splits) bytes, not overlapping
  * any input or output; its contents are overwritten.  1 <= n_splits <= 256.
- * Two kernels are enqueued on `stream`; nothing is allocated.  Other arguments,
+ * Two kernels are enqueued on `stream` (one when n_splits == 1: the plain
+ * forward, which gives the same values, and the workspace is left untouched);
+ * nothing is allocated.  Other arguments,
  * layouts and status codes as attn_fwd (ATTN_ERR_INVALID_ARG also for a
  * too-small workspace).
  */
@@ -118,9 +120,11 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
    alignment; 0 for invalid sizes.  Host only, no CUDA call. */
 size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Sq, int D, int n_splits);
 
-/* A split count for the current device: 1 when B*Hq*ceil(Sq/256) work items
-   already fill its SMs, else enough ranges for about two items per SM, with at
-   least four 128-key tiles per range. */
+/* A split count for the current device, from a cost model of the launch on
+   GB300: the work items of every split count run in waves over the SMs (so a
+   split that fills the last wave can pay even when the items already outnumber
+   the SMs), against the merge's extra traffic; at least four 128-key tiles per
+   range, and 1 unless a split is predicted to gain at least 3 %. */
 int attn_fwd_splitkv_suggest(int B, int Hq, int Sq, int Sk, int D, int causal);
 
 /*

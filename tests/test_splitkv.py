@@ -82,3 +82,28 @@ def test_workspace_checks():
     st = ops.load().attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                      1, 2, 1, 128, 1000, 64, 0, 0.125, 4, None, need, None)
     assert st == ops.ATTN_ERR_NULL_PTR
+
+
+def test_suggested_split_of_an_equal_item_workload_matches_the_oracle():
+    # 512 equal work items on the GPU's SMs leave the last wave partly filled; the suggestion splits the keys
+    # (the chunked-prefill shape at D = 64: 8 x 32 query heads, 512 rows, 16384 keys, bottom-right causal)
+    B, Hq, Hkv, Sq, Sk, D = 8, 32, 8, 512, 16384, 64
+    splits = ops.splitkv_suggest(B, Hq, Sq, Sk, D, 1)
+    assert splits > 1
+    q, k, v = draw(B, Hq, Hkv, Sq, Sk, D, seed=35)
+    o, lse = ops.attn_fwd_splitkv(q.cuda(), k.cuda(), v.cuda(), causal=1, n_splits=splits)
+    rows = sample_rows(B, Hq, Sq, 3, seed=36)
+    scale = float(np.float32(D ** -0.5))
+    o_ref, lse_ref = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), 1, scale, rows=rows)
+    idx = torch.from_numpy(rows)
+    compare(o.cpu().reshape(-1, D)[idx], lse.cpu().reshape(-1)[idx], o_ref, lse_ref)
+
+
+def test_one_split_is_the_plain_forward_bit_for_bit():
+    q, k, v = [t.cuda() for t in draw(2, 8, 2, 700, 1500, 128, seed=37)]
+    o1, l1 = ops.attn_fwd(q, k, v, causal=1)
+    ws = torch.full((ops.splitkv_workspace_size(2, 8, 700, 128, 1),), 7, dtype=torch.uint8, device="cuda")
+    o2, l2 = ops.attn_fwd_splitkv(q, k, v, causal=1, n_splits=1, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert bool((ws == 7).all())  # one range needs no partials
