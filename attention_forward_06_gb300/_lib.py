@@ -16,8 +16,8 @@ _libs: dict[str, ctypes.CDLL] = {}
 
 _c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
 
-# name -> (restype, argtypes), mirroring include/attn_fwd.h, include/attn_fwd_trace.h, include/attn_bwd.h and
-# include/attn_fwd_probe.h
+# name -> (restype, argtypes), mirroring include/attn_fwd.h, include/attn_fwd_trace.h, include/attn_bwd.h,
+# include/attn_bwd_trace.h and include/attn_fwd_probe.h
 SIGNATURES = {
     "attn_fwd": {
         "attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
@@ -54,6 +54,9 @@ SIGNATURES = {
 SIGNATURES["attn_fwd_trace"] = dict(SIGNATURES["attn_fwd"])
 SIGNATURES["attn_fwd_trace"]["attn_fwd_trace_read"] = (
     _c_int, [_vp, ctypes.c_size_t, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)])
+SIGNATURES["attn_bwd_trace"] = dict(SIGNATURES["attn_bwd"])
+SIGNATURES["attn_bwd_trace"]["attn_bwd_trace_read"] = (
+    _c_int, [_vp, ctypes.c_size_t] + [ctypes.POINTER(_c_int)] * 4)
 
 
 class LibraryMissing(RuntimeError):

@@ -3,6 +3,7 @@
     libattn_fwd.so        the attention forward pass (C ABI: include/attn_fwd.h)
     libattn_fwd_trace.so  the same with the kernel's timeline recorded (-DATTN_TRACE; include/attn_fwd_trace.h)
     libattn_bwd.so        its backward (C ABI: include/attn_bwd.h)
+    libattn_bwd_trace.so  the same with the backward kernels' timeline recorded (-DATTN_TRACE; include/attn_bwd_trace.h)
     libattn_probe.so      primitive checks of their building blocks (include/attn_fwd_probe.h)
 
 The translation units compile in parallel; a library is rebuilt only when a
@@ -33,6 +34,7 @@ LIBS = {  # name -> (source, extra nvcc flags)
     "attn_fwd": (os.path.join(CSRC, "attn_fwd.cu"), []),
     "attn_fwd_trace": (os.path.join(CSRC, "attn_fwd.cu"), ["-DATTN_TRACE"]),
     "attn_bwd": (os.path.join(CSRC, "attn_bwd.cu"), []),
+    "attn_bwd_trace": (os.path.join(CSRC, "attn_bwd.cu"), ["-DATTN_TRACE"]),
     "attn_probe": (os.path.join(CSRC, "probe.cu"), []),
 }
 

@@ -88,6 +88,48 @@ struct BParams {
 
 __device__ int g_bwd_status;
 
+#ifdef ATTN_TRACE
+// Timeline build (-DATTN_TRACE, off by default): lane 0 of each role of the dK/dV
+// kernel (kernel 0) and the dQ kernel (kernel 1) records (%globaltimer, event,
+// argument) at the points listed in attn_bwd_trace.h, in a fixed device array that
+// attn_bwd_trace_read copies out.  Without the switch every trace point compiles to
+// nothing.
+constexpr int kTraceKernels = 2;    // dK/dV, dQ
+constexpr int kTraceRoles = 4;      // producer, issuer, compute warpgroup 0, compute warpgroup 1
+constexpr int kTraceEvents = 2048;  // per role and CTA; later events are counted but not kept
+constexpr int kTraceCtas = 160;     // CTAs numbered past this are not recorded
+struct TraceRec {
+  unsigned long long t;
+  unsigned int code;
+  unsigned int arg;
+};
+__device__ TraceRec g_btrace[kTraceKernels * kTraceCtas * kTraceRoles * kTraceEvents];
+__device__ unsigned int g_btrace_n[kTraceKernels * kTraceCtas * kTraceRoles];
+struct Tracer {
+  int slot;  // (kernel * kTraceCtas + CTA) * kTraceRoles + role, or -1 when not recording
+  unsigned int n;
+  __device__ __forceinline__ void rec(unsigned int code, unsigned int arg) {
+    if (slot < 0) return;
+    if (n < kTraceEvents) g_btrace[static_cast<size_t>(slot) * kTraceEvents + n] = TraceRec{global_timer_ns(), code, arg};
+    ++n;
+  }
+  __device__ __forceinline__ void done() {
+    if (slot >= 0) g_btrace_n[slot] = n;
+  }
+};
+__device__ __forceinline__ int trace_slot(int kernel, int role, bool on) {
+  return (on && blockIdx.x < kTraceCtas) ? (kernel * kTraceCtas + static_cast<int>(blockIdx.x)) * kTraceRoles + role
+                                         : -1;
+}
+#define ATTN_TR_DECL(kernel, role, on) Tracer tr_{trace_slot((kernel), (role), (on)), 0u}
+#define ATTN_TR(code, arg) tr_.rec((code), static_cast<unsigned int>(arg))
+#define ATTN_TR_DONE() tr_.done()
+#else
+#define ATTN_TR_DECL(kernel, role, on) ((void)0)
+#define ATTN_TR(code, arg) ((void)0)
+#define ATTN_TR_DONE() ((void)0)
+#endif
+
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
@@ -260,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     // The prep kernel's vectors are complete before the first load; then the dQ
     // kernel may be scheduled (its CTAs take the SMs this kernel's CTAs leave).
+    ATTN_TR_DECL(0, 0, lane == 0);
+    ATTN_TR(0, 0);  // CTA start
     griddep_wait();
     griddep_launch_dependents();
     uint32_t it = 0, n_ne = 0;  // ring loads issued; items with query tiles
@@ -273,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nI <= 0) continue;
       if (n_ne > 0) ok = warp_wait(&kv_empty, (n_ne - 1) & 1, abort_v, kTimeoutNs);
       if (!ok) break;
+      ATTN_TR(1, x);  // the item's K and V loads issued
       mbar_arrive_expect_tx_elect(&kv_full, 2 * C::kTileBytes);
 #pragma unroll
       for (int cb = 0; cb < D / 64; ++cb) {
@@ -305,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(&full[u % kRing], (u / kRing) & 1, abort_v, kDrainTimeoutNs);
       if (n_ne > 0) mbar_wait_bounded(&kv_full, (n_ne - 1) & 1, abort_v, kDrainTimeoutNs);
     }
+    ATTN_TR_DONE();
    } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tcgen05 issuer
     constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BH2, false);  // M = 128 keys, N = 64 query rows
@@ -333,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_bf16_ts_k4(tmem + 2 * BT, tmem + 128 * r, dob, idesc_acc, acc);
       mma_bf16_ts_k4(tmem + 3 * BT, tmem + 128 * r + BH2, qb, idesc_acc, acc, bar0, bar1);
     };
+    ATTN_TR_DECL(0, 1, lane == 0);
     uint32_t it = 0, g = 0, n_ne = 0;  // ring uses, steps (st/pt phases), items with query tiles
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
@@ -346,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = warp_wait(&full[it % kRing], (it / kRing) & 1, abort_v, kTimeoutNs);
       if (!ok) break;
       tc_fence_after();
+      ATTN_TR(10, x);  // the item's first S-type products
       issue_s(0, it % kRing);
       issue_s(1, it % kRing);
       // K and V are read only by the S-type products: the next item's K and V may load
@@ -359,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         issue_acc(0, slot, s > 0 ? 1u : 0u, kNoBar, kNoBar);
+        ATTN_TR(11, s);  // half 0's dV and dK products of step s
         if (more) {
           ok = warp_wait(&full[next], ((it + 1) / kRing) & 1, abort_v, kTimeoutNs);
           if (!ok) break;
@@ -379,6 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
     mma_commit_elect(&drain);
     warp_wait(&drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
+    ATTN_TR(13, 0);  // every MMA of the CTA completed
+    ATTN_TR_DONE();
    }
   } else {
     // ------------------------------------------------------------ compute (one thread per key)
@@ -392,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t st_t = tmem + lane_off + 128 * r, dpt_t = st_t + BH2;
     const uint32_t acc_t = tmem + lane_off + (r == 0 ? 2 * BT : 3 * BT);
     const int kk = quarter * 32 + lane;
+    ATTN_TR_DECL(0, 2 + r, quarter == 0 && lane == 0);
     uint32_t it = 0, g = 0, n_ne = 0;
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
@@ -421,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = warp_wait(&full[it % kRing], (it / kRing) & 1, abort_v, kTimeoutNs);
         if (ok) ok = warp_wait(&st_full[r], g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
+        ATTN_TR(20, s);  // S^T_r and dP^T_r of step s ready
         tc_fence_after();
         uint32_t sv[64], dpv[64];
         tmem_ld2x64_wait(st_t, dpt_t, sv, dpv);
@@ -459,12 +512,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&pt_full[r]);
+        ATTN_TR(21, s);  // P^T_r and dS^T_r handed to the MMA
       }
       if (!ok) break;
       // epilogue: dV (warpgroup 0) or scale * dK (warpgroup 1) of this key, bf16, once the
       // item's MMAs are done
       ok = warp_wait(&acc_full, n_ne & 1, abort_v, kTimeoutNs);
       if (!ok) break;
+      ATTN_TR(23, x);  // the item's dV and dK complete: epilogue starts
       ++n_ne;
       tc_fence_after();
       const float mul = r == 0 ? 1.0f : p.scale;
@@ -482,8 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&acc_empty);  // dV and dK may be overwritten by the next item
+      ATTN_TR(24, x);  // epilogue done
     }
     if (!ok && lane == 0) record_abort(abort_v, kSiteCompute);
+    ATTN_TR_DONE();
   }
 
   tc_fence_before();
@@ -578,6 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1)
    regs_decrease<kRegsOther>();
    if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
+    ATTN_TR_DECL(1, 0, lane == 0);
+    ATTN_TR(0, 0);  // CTA start
     uint32_t kl = 0, vl = 0, n_ne = 0;  // K and V tiles loaded; items with key tiles
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
@@ -588,6 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n <= 0) continue;
       if (n_ne > 0) ok = warp_wait(&qd_empty, (n_ne - 1) & 1, abort_v, kTimeoutNs);
       if (!ok) break;
+      ATTN_TR(1, x);  // the item's Q and dO loads issued
       mbar_arrive_expect_tx_elect(&qd_full, 2 * C::kTileBytes);
 #pragma unroll
       for (int cb = 0; cb < D / 64; ++cb) {
@@ -625,8 +685,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(&vfull[u % VR], (u / VR) & 1, abort_v, kDrainTimeoutNs);
       if (n_ne > 0) mbar_wait_bounded(&qd_full, (n_ne - 1) & 1, abort_v, kDrainTimeoutNs);
     }
+    ATTN_TR_DONE();
    } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tcgen05 issuer
+    ATTN_TR_DECL(1, 1, lane == 0);
     constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, false);  // M = 128 rows, N = 128 keys
     constexpr uint32_t idesc_acc = idesc_bf16_f32(BT, D, true);  // M = 128 rows, N = D, B MN-major
     constexpr uint32_t kDp = 2 * BT, kDq = 3 * BT;               // TMEM columns of dP and dQ
@@ -660,6 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!w) return false;
       tc_fence_after();
       mma_bf16_ts_k4(tmem + kDq, reg, sdesc_sw128(ka, BC::kColBlockBytes, 1024), idesc_acc, first ? 0u : 1u);
+      ATTN_TR(11, (first ? 0u : 1u) | (last ? 2u : 0u));  // half 0's dQ += dS K (arg: item's first, last)
       w = warp_wait(&ds_full[1][gg & 1], (gg >> 1) & 1, abort_v, kTimeoutNs);
       if (!w) return false;
       tc_fence_after();
@@ -686,6 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = warp_wait(&kfull[ks], (g / KR) & 1, abort_v, kTimeoutNs);
         if (!ok) break;
         tc_fence_after();
+        if (j == 0) ATTN_TR(10, x);  // the item's first S product
         issue_s(BT * (g & 1), ks);
         if (g > 0) ok = warp_wait(&dp_free, (g - 1) & 1, abort_v, kTimeoutNs);  // dP(g-1) read by all
         if (ok) ok = warp_wait(&vfull[vs], (g / VR) & 1, abort_v, kTimeoutNs);
@@ -706,6 +770,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) record_abort(abort_v, kSiteIssuer);
     mma_commit_elect(&drain);
     warp_wait(&drain, 0, abort_v, ok ? kTimeoutNs : kDrainTimeoutNs);
+    ATTN_TR(13, 0);  // every MMA of the CTA completed
+    ATTN_TR_DONE();
    }
   } else {
     // ------------------------------------------------------------ compute (one thread per query row)
@@ -715,6 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = warp / 4, quarter = warp % 4;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t dp_t = tmem + lane_off + 2 * BT + BH2 * r, dq_t = tmem + lane_off + 3 * BT;
+    ATTN_TR_DECL(1, 2 + r, quarter == 0 && lane == 0);
     uint32_t g = 0, t = 0;
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items && ok; ++k) {
@@ -740,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n; ++j, ++g) {
         ok = warp_wait(&st_full, g & 1, abort_v, kTimeoutNs);
         if (!ok) break;
+        ATTN_TR(20, j);  // S and dP of key tile j ready
         tc_fence_after();
         const uint32_t s_t = tmem + lane_off + BT * (g & 1) + BH2 * r;
         uint32_t sv[64], dpv[64];
@@ -767,10 +835,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&ds_full[r][g & 1]);
+        ATTN_TR(21, j);  // dS of this warpgroup's keys handed to the MMA
       }
       if (!ok) break;
       ok = warp_wait(&acc_full, t & 1, abort_v, kTimeoutNs);
       if (!ok) break;
+      ATTN_TR(23, x);  // the item's dQ complete: epilogue starts
       ++t;
       tc_fence_after();
       // the warp's 32 rows, this warpgroup's D/2 columns (D bytes) of each
@@ -790,8 +860,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&acc_empty);
+      ATTN_TR(24, x);  // epilogue done
     }
     if (!ok && lane == 0) record_abort(abort_v, kSiteCompute);
+    ATTN_TR_DONE();
   }
 
   tc_fence_before();
@@ -999,6 +1071,25 @@ const char* attn_bwd_strerror(int status) {
     default: return "unknown status";
   }
 }
+
+#ifdef ATTN_TRACE
+int attn_bwd_trace_read(void* dst, size_t dst_bytes, int* kernels, int* ctas, int* roles, int* events) {
+  if (kernels) *kernels = kTraceKernels;
+  if (ctas) *ctas = kTraceCtas;
+  if (roles) *roles = kTraceRoles;
+  if (events) *events = kTraceEvents;
+  const size_t n_bytes = sizeof(unsigned int) * kTraceKernels * kTraceCtas * kTraceRoles;
+  const size_t r_bytes = sizeof(TraceRec) * static_cast<size_t>(kTraceKernels) * kTraceCtas * kTraceRoles * kTraceEvents;
+  if (!dst) return ATTN_ERR_NULL_PTR;
+  if (dst_bytes < n_bytes + r_bytes) return ATTN_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(dst, g_btrace_n, n_bytes);
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(static_cast<uint8_t*>(dst) + n_bytes, g_btrace, r_bytes);
+  static const unsigned int zeros[kTraceKernels * kTraceCtas * kTraceRoles] = {};  // later launches start empty
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_btrace_n, zeros, n_bytes);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+#endif
 
 int attn_bwd_debug_status(cudaStream_t stream, int* site) {
   if (site) *site = 0;

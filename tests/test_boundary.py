@@ -14,7 +14,9 @@ from attention_forward_06_gb300 import _lib, ops
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADERS = {"attn_fwd": "include/attn_fwd.h", "attn_fwd_trace": "include/attn_fwd_trace.h",
-           "attn_bwd": "include/attn_bwd.h", "attn_probe": "include/attn_fwd_probe.h"}
+           "attn_bwd": "include/attn_bwd.h", "attn_bwd_trace": "include/attn_bwd_trace.h",
+           "attn_probe": "include/attn_fwd_probe.h"}
+TRACED = {"attn_fwd_trace": "attn_fwd", "attn_bwd_trace": "attn_bwd"}  # traced build -> the library it extends
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,18 +37,19 @@ def test_library_exports_every_declared_symbol(name, built):
     lib = ctypes.CDLL(built[name])
     for f in funcs:
         assert hasattr(lib, f), f"{f} declared in {HEADERS[name]} but not exported"
-    # and the Python binding knows exactly these signatures (the traced build exports attn_fwd.h's as well)
+    # and the Python binding knows exactly these signatures (a traced build exports its library's as well)
     expected = set(funcs)
-    if name == "attn_fwd_trace":
-        expected |= set(declared_functions(HEADERS["attn_fwd"]))
-        for f in declared_functions(HEADERS["attn_fwd"]):
+    if name in TRACED:
+        expected |= set(declared_functions(HEADERS[TRACED[name]]))
+        for f in declared_functions(HEADERS[TRACED[name]]):
             assert hasattr(lib, f), f"{f} missing from the traced build"
     assert sorted(_lib.SIGNATURES[name]) == sorted(expected)
 
 
-def test_default_build_records_no_timeline(built):
-    lib = ctypes.CDLL(built["attn_fwd"])
-    for f in declared_functions(HEADERS["attn_fwd_trace"]):
+@pytest.mark.parametrize("traced", sorted(TRACED))
+def test_default_build_records_no_timeline(traced, built):
+    lib = ctypes.CDLL(built[TRACED[traced]])
+    for f in declared_functions(HEADERS[traced]):
         assert not hasattr(lib, f), f"{f} is exported by the default build"
 
 
