@@ -64,6 +64,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <atomic>
 #include <mutex>
@@ -161,12 +162,21 @@ struct Item {
 };
 
 // Item x of the heaviest-first list: query block from the last, then (split-key
-// mode) the key range, heads fastest.
-template <bool SPLIT, bool SPARSE = false>
+// mode) the key range, heads fastest.  Grouped order (GROUPED, dense mode): the
+// G x n_qblocks items that read one kv head's K and V are adjacent -- kv heads in
+// order, then query blocks from the last, the group's query heads fastest -- so
+// they run in the same wave and share each K and V tile through L2.
+template <bool SPLIT, bool SPARSE = false, bool GROUPED = false>
 __device__ __forceinline__ Item item_at(const Params& p, int x) {
   Item it;
   int qb, r;
-  if (SPLIT) {
+  if constexpr (GROUPED) {
+    const int per = p.G * p.n_qblocks;  // items of one kv head
+    const int grp = x / per, w = x % per;
+    qb = p.n_qblocks - 1 - w / p.G;
+    it.bh = (grp / p.Hkv) * p.Hq + (grp % p.Hkv) * p.G + w % p.G;
+    it.split = 0;
+  } else if (SPLIT) {
     const int per = p.BH * p.n_splits;
     qb = p.n_qblocks - 1 - x / per;
     r = x % per;
@@ -384,7 +394,7 @@ __device__ __forceinline__ void record_abort(volatile uint32_t* abort_flag, int 
   atomicCAS(&g_status, 0, site);
 }
 
-template <int D, bool SPLIT, bool SPARSE, bool ORDERED = false>
+template <int D, bool SPLIT, bool SPARSE, bool ORDERED = false, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -395,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // publishes the count with the item; every role walks the same tile sequence
   constexpr bool LISTED = SPARSE || ORDERED;
   static_assert(!(SPARSE && ORDERED) && !(SPLIT && (SPARSE || ORDERED)), "one visiting mode at a time");
+  static_assert(!GROUPED || !(SPLIT || SPARSE || ORDERED), "the grouped order is for the dense kernel");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint8_t* q_s = smem;               // Q tile t at q_s + t * kTileBytes
@@ -489,9 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int n_marked = 0;  // block-sparse / ordered mode: the key tiles the item visits
       if constexpr (SPARSE) {
-        if (more) n_marked = sparse_tiles(p, item_at<SPLIT, SPARSE>(p, x));
+        if (more) n_marked = sparse_tiles(p, item_at<SPLIT, SPARSE, GROUPED>(p, x));
       } else if constexpr (ORDERED) {
-        if (more) n_marked = ordered_tiles(p, item_at<SPLIT>(p, x));
+        if (more) n_marked = ordered_tiles(p, item_at<SPLIT, false, GROUPED>(p, x));
       }
       if (lane == 0) {
         item_seq[k % kSeqSlots] = more ? x : -1;
@@ -501,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       ATTN_TR(1, more ? x : -1);  // item published
       if (!more) break;
-      const Item it = item_at<SPLIT, SPARSE>(p, x);
+      const Item it = item_at<SPLIT, SPARSE, GROUPED>(p, x);
       const int n_tiles = LISTED ? n_marked : it.n_tiles;
       // The next item is claimed once this item's loads are all issued (about two
       // key tiles before its end), so items are handed out in the order CTAs free up.
@@ -632,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int x, n_marked = 0;
       ok = next_item(k, x, LISTED ? &n_marked : nullptr);
       if (!ok || x < 0) break;
-      const int n = LISTED ? n_marked : item_at<SPLIT>(p, x).n_tiles;
+      const int n = LISTED ? n_marked : item_at<SPLIT, false, GROUPED>(p, x).n_tiles;
       if (n == 0) continue;
       ok = warp_wait(&q_full, n_done & 1, abort_v, kTimeoutNs);
       if (ok) ok = wait_kv(kv_it);
@@ -756,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = next_item(k, x, LISTED ? &n_marked : nullptr);
       if (!ok || x < 0) break;
       if constexpr (!SPLIT) {  // split-key partials are written by the softmax warps directly
-        const Item it = item_at<SPLIT, SPARSE>(p, x);
+        const Item it = item_at<SPLIT, SPARSE, GROUPED>(p, x);
         if ((LISTED ? n_marked : it.n_tiles) == 0) continue;
         for (int t = 0; t < QTILES && ok; ++t) {
           ok = warp_wait(&stage_full[t], e_seen[t] & 1, abort_v, kTimeoutNs);
@@ -801,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (x < 0) break;
-      const Item it = item_at<SPLIT, SPARSE>(p, x);
+      const Item it = item_at<SPLIT, SPARSE, GROUPED>(p, x);
       const int n_tiles = LISTED ? n_marked : it.n_tiles;  // key tiles the item visits
       const int row = it.q0 + t * BM + quarter * 32 + lane;  // global query row
       const bool live = row < p.Sq;
@@ -1210,6 +1221,7 @@ std::atomic<unsigned int> g_capture_seq{0};  // picks each captured launch's sch
 std::mutex g_dev_mutex;
 int g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 unsupported
 int g_dev_sms[kMaxDevices];    // streaming multiprocessors per device
+int64_t g_dev_l2[kMaxDevices];  // L2 bytes per device
 
 // Capability check and kernel attributes, once per device.
 int prepare_device(int dev) {
@@ -1229,14 +1241,20 @@ int prepare_device(int dev) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e);
   g_dev_sms[dev] = sms;
+  int l2 = 0;
+  e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_dev_l2[dev] = l2;
   const void* k128[] = {reinterpret_cast<const void*>(attn_fwd_kernel<128, false, false>),
                         reinterpret_cast<const void*>(attn_fwd_kernel<128, true, false>),
                         reinterpret_cast<const void*>(attn_fwd_kernel<128, false, true>),
-                        reinterpret_cast<const void*>(attn_fwd_kernel<128, false, false, true>)};
+                        reinterpret_cast<const void*>(attn_fwd_kernel<128, false, false, true>),
+                        reinterpret_cast<const void*>(attn_fwd_kernel<128, false, false, false, true>)};
   const void* k64[] = {reinterpret_cast<const void*>(attn_fwd_kernel<64, false, false>),
                        reinterpret_cast<const void*>(attn_fwd_kernel<64, true, false>),
                        reinterpret_cast<const void*>(attn_fwd_kernel<64, false, true>),
-                       reinterpret_cast<const void*>(attn_fwd_kernel<64, false, false, true>)};
+                       reinterpret_cast<const void*>(attn_fwd_kernel<64, false, false, true>),
+                       reinterpret_cast<const void*>(attn_fwd_kernel<64, false, false, false, true>)};
   for (const void* f : k128)
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<128>::kSmemBytes);
@@ -1312,6 +1330,7 @@ struct Launch {
   int grid = 0;
   int dev = 0;
   bool empty = false;  // B == 0 or Sq == 0: nothing to do
+  bool grouped = false;  // dense mode: items in the grouped order (see item_at)
 };
 
 int prepare_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
@@ -1397,15 +1416,42 @@ int prepare_launch(const void* q, const void* k, const void* v, void* o, float* 
   prm.n_qtiles = static_cast<int>((Sq + BM - 1) / BM);
   // persistent: one CTA per SM (shared memory and TMEM allow no second), never more CTAs than items
   L->grid = static_cast<int>(items < g_dev_sms[L->dev] ? items : g_dev_sms[L->dev]);
+  // The grouped item order, when K and V of all kv heads do not fit in L2 (in the heads-fastest order each
+  // kv head's items fall into different waves, so its tiles come from HBM once per wave), the items of one
+  // kv head fit in one wave, and the items are about equally long (the grouped order is heaviest first only
+  // within a kv head).
+  {
+    const int64_t per = static_cast<int64_t>(Hq / Hkv) * n_qblocks;
+    const int64_t kv_bytes = 2 * kv_elems * 2;
+    auto key_tiles = [&](int64_t qb) {  // key tiles of query block qb under the mask
+      int64_t kv_end = Sk;
+      if (causal) kv_end = std::min<int64_t>(Sk, std::min<int64_t>((qb + 1) * ROWS_PER_ITEM, Sq) - 1 + prm.diag + 1);
+      return kv_end > 0 ? (kv_end + BN - 1) / BN : 0;
+    };
+    const int64_t t_min = key_tiles(0), t_max = key_tiles(n_qblocks - 1);
+    L->grouped = n_splits == 1 && per >= 2 && per <= L->grid && kv_bytes > g_dev_l2[L->dev] &&
+                 10 * t_min >= 9 * t_max;
+    // ATTN_FWD_ITEM_ORDER=heads or =grouped overrides the choice (the results are the same bit for bit)
+    const char* order = std::getenv("ATTN_FWD_ITEM_ORDER");
+    if (order && std::strcmp(order, "heads") == 0) L->grouped = false;
+    if (order && std::strcmp(order, "grouped") == 0) L->grouped = n_splits == 1;
+  }
   return ATTN_OK;
 }
 
-template <int D, bool SPLIT, bool SPARSE = false, bool ORDERED = false>
+template <int D, bool SPLIT, bool SPARSE = false, bool ORDERED = false, bool GROUPED = false>
 int launch(const Launch& L, cudaStream_t stream) {
-  attn_fwd_kernel<D, SPLIT, SPARSE, ORDERED><<<L.grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(L.tq, L.tk, L.tv,
-                                                                                              L.to, L.prm);
+  attn_fwd_kernel<D, SPLIT, SPARSE, ORDERED, GROUPED><<<L.grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(
+      L.tq, L.tk, L.tv, L.to, L.prm);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+// The dense kernel in the item order prepare_launch chose.
+int launch_dense(const Launch& L, int D, cudaStream_t stream) {
+  if (L.grouped)
+    return D == 128 ? launch<128, false, false, false, true>(L, stream) : launch<64, false, false, false, true>(L, stream);
+  return D == 128 ? launch<128, false>(L, stream) : launch<64, false>(L, stream);
 }
 
 template <int D>
@@ -1421,7 +1467,7 @@ int launch_merge(const Launch& L, int64_t rows, cudaStream_t stream) {
 // One range is the plain forward: the merge of a single partial multiplies it by
 // exactly 1, so the plain kernel writes the same values without the partials.
 int run_splitkv(const Launch& L0, void* ws, int64_t rows, int D, cudaStream_t stream) {
-  if (L0.prm.n_splits == 1) return D == 128 ? launch<128, false>(L0, stream) : launch<64, false>(L0, stream);
+  if (L0.prm.n_splits == 1) return launch_dense(L0, D, stream);
   Launch L = L0;
   size_t lse_off = 0;
   splitkv_bytes(rows, D, L.prm.n_splits, &lse_off);
@@ -1501,7 +1547,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   Launch L;
   const int st = prepare_launch(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, 1, stream, &L);
   if (st != ATTN_OK || L.empty) return st;
-  return D == 128 ? launch<128, false>(L, stream) : launch<64, false>(L, stream);
+  return launch_dense(L, D, stream);
 }
 
 size_t attn_fwd_splitkv_workspace_size(int B, int Hq, int Sq, int D, int n_splits) {

@@ -257,3 +257,22 @@ def test_v_beyond_fp16_range_is_clamped_and_leaves_other_rows_exact():
     # the other columns of the rows that see the key are unaffected as well
     keep = [c for c in range(128) if c != 5]
     compare(o[:, :, 200:, keep].contiguous(), lse[:, :, 200:], o_ref[:, :, 200:, keep], lse_ref[:, :, 200:])
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,D,causal", [
+    (2, 8, 2, 512, 3000, 128, 1),   # chunked-prefill shape: 8 items per kv head
+    (1, 4, 4, 700, 700, 64, 2),     # ragged, no grouping of heads (G = 1)
+    (3, 6, 2, 300, 1000, 128, 0),   # non-causal, G = 3
+])
+def test_item_orders_give_identical_results(B, Hq, Hkv, Sq, Sk, D, causal, monkeypatch):
+    """The grouped item order (a kv head's items handed out together) computes every output element exactly as
+    the heads-fastest order does; both match the oracle."""
+    q, k, v = draw(B, Hq, Hkv, Sq, Sk, D, seed=Sq + Sk)
+    scale = float(np.float32(D ** -0.5))
+    outs = {}
+    for order in ("heads", "grouped"):
+        monkeypatch.setenv("ATTN_FWD_ITEM_ORDER", order)
+        outs[order] = run_gpu(q, k, v, causal, scale)
+    assert torch.equal(outs["heads"][0], outs["grouped"][0]) and torch.equal(outs["heads"][1], outs["grouped"][1])
+    o_ref, lse_ref = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal, scale)
+    compare(*outs["grouped"], o_ref, lse_ref, label=f"order {B}x{Hq}x{Hkv}x{Sq}x{Sk}x{D}x{causal}")
