@@ -39,12 +39,12 @@
  *
  * Work order.  A launch's work items (256 query rows of one head) are handed to
  * the CTAs heaviest first with heads fastest.  When K and V of all kv heads
- * exceed the L2 cache, the items of one kv head fit in one wave of CTAs and the
- * items are about equally long (chunked prefill over a long context), the
- * items of each kv head are handed out together instead, so that they read each
- * K and V tile from HBM once.  The order never changes the results: every output
- * element is computed the same way in either order.  The environment variable
- * ATTN_FWD_ITEM_ORDER=heads or =grouped, read at each call, forces one order.
+ * exceed the L2 cache (long contexts, chunked prefill over them), the items of
+ * each kv head are handed out together instead, heaviest first within the kv
+ * head, so that K and V tiles are not read again from HBM wave after wave.  The
+ * order never changes the results: every output element is computed the same
+ * way in either order.  The environment variable ATTN_FWD_ITEM_ORDER=heads or
+ * =grouped, read at each call, forces one order.
  *
  * Concurrency.  Each forward launch (attn_fwd and every variant below) claims
  * its work items from one of a set of device counters and returns that counter
