@@ -5,9 +5,11 @@
 //
 // Persistent kernel: one CTA per SM walks a list of work items, each 256 query
 // rows (two 128-row Q tiles) of one (batch, query head).  Items are ordered
-// heaviest first (most key tiles under a causal mask); CTA c starts on item c
-// and claims later items from a counter as it frees up, so the CTAs end within
-// about one small item of each other.  Twelve warps:
+// heaviest first (most key tiles under a causal mask), heads fastest -- or, in
+// the grouped instantiation the host picks when K and V exceed L2, kv head by kv
+// head, heaviest first within each; CTA c starts on item c and claims later
+// items from a counter as it frees up, so the CTAs end within about one small
+// item of each other.  Twelve warps:
 //   warps 0-3   softmax for Q tile 0 (one thread per query row), then its epilogue
 //   warps 4-7   softmax for Q tile 1, then its epilogue
 //   warp  8     TMA producer: the Q tiles of an item, then its K/V tiles through a

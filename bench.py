@@ -24,6 +24,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -199,6 +200,20 @@ def time_kernel(fn, steps: int, warmup: int, flush: torch.Tensor, stream) -> lis
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def kernel_code_sha256(sources=None) -> str:
+    """sha256 of the forward kernel's sources with comments and blank lines removed: the key of the DRAM traffic
+    record, which a change to the code invalidates and a change to a comment does not."""
+    h = hashlib.sha256()
+    for src in sources or [os.path.join(ROOT, s) for s in KERNEL_SOURCES]:
+        with open(src) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())
+        h.update(b"\0")
+    return h.hexdigest()
+
+
 def traffic_for(workload: str):
     """DRAM bytes per launch from a committed ncu capture, or None if absent or the kernel changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -207,12 +222,8 @@ def traffic_for(workload: str):
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    h = hashlib.sha256()
-    for src in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, src), "rb") as f:
-            h.update(f.read())
     entry = rec.get(workload)
-    if not entry or entry.get("kernel_sha256") != h.hexdigest():
+    if not entry or entry.get("kernel_sha256") != kernel_code_sha256():
         return None
     return entry.get("dram_bytes_per_launch")
 

@@ -84,3 +84,22 @@ def test_flop_conventions_on_the_benchmark_workloads():
                      ("long", 1350.6)):
         assert bench.min_hbm_bytes(WORKLOADS[name]) / 1e6 == pytest.approx(mb, abs=0.05)
     assert bench.alg_flops(WORKLOADS["tiny"]) == bench.conv_flops(WORKLOADS["tiny"])
+
+
+def test_traffic_record_key_ignores_comments_and_tracks_code(tmp_path):
+    """The DRAM traffic record is keyed to the kernel's code: editing a comment keeps the key, editing code
+    changes it."""
+    src = tmp_path / "k.cu"
+    src.write_text("// a comment\nint f(int x) {\n  return x + 1;  // trailing\n}\n/* block\n comment */\n")
+    base = bench.kernel_code_sha256([str(src)])
+    src.write_text("// another comment\n\nint f(int x) {\n  return x + 1;  // changed\n}\n")
+    assert bench.kernel_code_sha256([str(src)]) == base
+    src.write_text("int f(int x) {\n  return x + 2;\n}\n")
+    assert bench.kernel_code_sha256([str(src)]) != base
+
+
+def test_committed_traffic_record_is_for_the_current_kernel():
+    """Every performance workload has a DRAM traffic record taken on the kernel code as it stands, so the
+    benchmark line carries measured traffic (a kernel change without a new capture fails here)."""
+    for name in bench.PERF_WORKLOADS:
+        assert bench.traffic_for(name), f"no current traffic record for {name}"
