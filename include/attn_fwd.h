@@ -38,13 +38,14 @@
  * entry point, per-device capability check and kernel attributes) is guarded.
  *
  * Work order.  A launch's work items (256 query rows of one head) are handed to
- * the CTAs heaviest first with heads fastest.  When K and V of all kv heads
- * exceed the L2 cache (long contexts, chunked prefill over them), the items of
- * each kv head are handed out together instead, heaviest first within the kv
- * head, so that K and V tiles are not read again from HBM wave after wave.  The
- * order never changes the results: every output element is computed the same
- * way in either order.  The environment variable ATTN_FWD_ITEM_ORDER=heads or
- * =grouped, read at each call, forces one order.
+ * the CTAs heaviest first with heads fastest.  In the dense forward (attn_fwd,
+ * and attn_fwd_splitkv with one split), when K and V of all kv heads exceed the
+ * L2 cache (long contexts, chunked prefill over them), the items of each kv head
+ * are handed out together instead, heaviest first within the kv head, so that K
+ * and V tiles are not read again from HBM wave after wave.  The order never
+ * changes the results: every output element is computed the same way in either
+ * order.  The environment variable ATTN_FWD_ITEM_ORDER=heads or =grouped, read
+ * at each call, forces one order.
  *
  * Concurrency.  Each forward launch (attn_fwd and every variant below) claims
  * its work items from one of a set of device counters and returns that counter
