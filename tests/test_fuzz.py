@@ -4,7 +4,7 @@ Each case draws batch, heads (grouped-query ratios 1 to 8), ragged lengths up to
 600, D in {64, 128}, all three causal modes, a positive scale around 1/sqrt(D)
 and a logit spread from soft to sharply peaked; it runs the plain forward, one of
 the split-key, block-sparse or ordered forwards (chosen by the case), and on every
-third case the backward, each compared with the oracle's result for the same
+third case the backward (odd cases run the dense forward in the grouped item order), each compared with the oracle's result for the same
 inputs (the ordered forward with a random permutation is plain attention; the
 block-sparse one is compared with the oracle's block-mask path).
 """
@@ -49,8 +49,12 @@ def check_grad(name, g, ref):
 
 
 @pytest.mark.parametrize("i", range(N_CASES))
-def test_random_case(i):
+def test_random_case(i, monkeypatch):
     c = case_params(i)
+    # half the cases run the dense forward in the grouped item order (a kv head's items together), which the
+    # library otherwise picks only for K and V larger than L2
+    if i % 2:
+        monkeypatch.setenv("ATTN_FWD_ITEM_ORDER", "grouped")
     B, Hq, Hkv, Sq, Sk, D, causal, scale = (c[k] for k in ("B", "Hq", "Hkv", "Sq", "Sk", "D", "causal", "scale"))
     q, k, v = draw(B, Hq, Hkv, Sq, Sk, D, c["seed"], qk_std=c["qk_std"])
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
