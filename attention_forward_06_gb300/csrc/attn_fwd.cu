@@ -164,10 +164,11 @@ struct Item {
 };
 
 // Item x of the heaviest-first list: query block from the last, then (split-key
-// mode) the key range, heads fastest.  Grouped order (GROUPED, dense mode): the
-// G x n_qblocks items that read one kv head's K and V are adjacent -- kv heads in
-// order, then query blocks from the last, the group's query heads fastest -- so
-// they run in the same wave and share each K and V tile through L2.
+// mode) the key range, heads fastest.  Grouped order (GROUPED; dense, block-sparse
+// and ordered modes): the G x n_qblocks items that read one kv head's K and V are
+// adjacent -- kv heads in order, then query blocks from the last, the group's
+// query heads fastest -- so they run side by side and share each K and V tile
+// through L2.
 template <bool SPLIT, bool SPARSE = false, bool GROUPED = false>
 __device__ __forceinline__ Item item_at(const Params& p, int x) {
   Item it;
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // publishes the count with the item; every role walks the same tile sequence
   constexpr bool LISTED = SPARSE || ORDERED;
   static_assert(!(SPARSE && ORDERED) && !(SPLIT && (SPARSE || ORDERED)), "one visiting mode at a time");
-  static_assert(!GROUPED || !(SPLIT || SPARSE || ORDERED), "the grouped order is for the dense kernel");
+  static_assert(!GROUPED || !SPLIT, "the grouped order lists whole-key-range items");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint8_t* q_s = smem;               // Q tile t at q_s + t * kTileBytes
@@ -1251,12 +1252,16 @@ int prepare_device(int dev) {
                         reinterpret_cast<const void*>(attn_fwd_kernel<128, true, false>),
                         reinterpret_cast<const void*>(attn_fwd_kernel<128, false, true>),
                         reinterpret_cast<const void*>(attn_fwd_kernel<128, false, false, true>),
-                        reinterpret_cast<const void*>(attn_fwd_kernel<128, false, false, false, true>)};
+                        reinterpret_cast<const void*>(attn_fwd_kernel<128, false, false, false, true>),
+                        reinterpret_cast<const void*>(attn_fwd_kernel<128, false, true, false, true>),
+                        reinterpret_cast<const void*>(attn_fwd_kernel<128, false, false, true, true>)};
   const void* k64[] = {reinterpret_cast<const void*>(attn_fwd_kernel<64, false, false>),
                        reinterpret_cast<const void*>(attn_fwd_kernel<64, true, false>),
                        reinterpret_cast<const void*>(attn_fwd_kernel<64, false, true>),
                        reinterpret_cast<const void*>(attn_fwd_kernel<64, false, false, true>),
-                       reinterpret_cast<const void*>(attn_fwd_kernel<64, false, false, false, true>)};
+                       reinterpret_cast<const void*>(attn_fwd_kernel<64, false, false, false, true>),
+                       reinterpret_cast<const void*>(attn_fwd_kernel<64, false, true, false, true>),
+                       reinterpret_cast<const void*>(attn_fwd_kernel<64, false, false, true, true>)};
   for (const void* f : k128)
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<128>::kSmemBytes);
@@ -1640,6 +1645,8 @@ int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, f
   L.prm.mask = block_mask;
   L.prm.mask_heads = mask_heads;
   L.prm.mask_words = static_cast<int>(((static_cast<int64_t>(Sk) + BN - 1) / BN + 31) / 32);
+  if (L.grouped)
+    return D == 128 ? launch<128, false, true, false, true>(L, stream) : launch<64, false, true, false, true>(L, stream);
   return D == 128 ? launch<128, false, true>(L, stream) : launch<64, false, true>(L, stream);
 }
 
@@ -1671,6 +1678,8 @@ int attn_fwd_ordered(const void* q, const void* k, const void* v, void* o, float
   L.prm.order = tile_order;
   L.prm.order_heads = order_heads;
   L.prm.order_len = static_cast<int>((static_cast<int64_t>(Sk) + BN - 1) / BN);
+  if (L.grouped)
+    return D == 128 ? launch<128, false, false, true, true>(L, stream) : launch<64, false, false, true, true>(L, stream);
   return D == 128 ? launch<128, false, false, true>(L, stream) : launch<64, false, false, true>(L, stream);
 }
 

@@ -276,3 +276,18 @@ def test_item_orders_give_identical_results(B, Hq, Hkv, Sq, Sk, D, causal, monke
     assert torch.equal(outs["heads"][0], outs["grouped"][0]) and torch.equal(outs["heads"][1], outs["grouped"][1])
     o_ref, lse_ref = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal, scale)
     compare(*outs["grouped"], o_ref, lse_ref, label=f"order {B}x{Hq}x{Hkv}x{Sq}x{Sk}x{D}x{causal}")
+    # the block-sparse and ordered forwards have the grouped order too
+    rng = np.random.default_rng(Sq + Sk)
+    blocks = torch.from_numpy(rng.random((B, Hq, -(-Sq // 128), -(-Sk // 128))) < 0.5)
+    words = ops.pack_block_mask(blocks).cuda()
+    tile_order = torch.from_numpy(np.stack([rng.permutation(-(-Sk // 128)) for _ in range(B * -(-Sq // 256))])
+                                  .reshape(B, 1, -(-Sq // 256), -(-Sk // 128)).astype(np.int32)).cuda()
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    for call in (lambda: ops.attn_fwd_blocksparse(qd, kd, vd, words, causal=causal, scale=scale),
+                 lambda: ops.attn_fwd_ordered(qd, kd, vd, tile_order, causal=causal, scale=scale)):
+        res = {}
+        for order in ("heads", "grouped"):
+            monkeypatch.setenv("ATTN_FWD_ITEM_ORDER", order)
+            res[order] = call()
+        torch.cuda.synchronize()
+        assert torch.equal(res["heads"][0], res["grouped"][0]) and torch.equal(res["heads"][1], res["grouped"][1])
